@@ -1,0 +1,188 @@
+/*
+ * moe.h - C ABI of the DeepSeekMoE layer forward for NVIDIA B300 (sm_103a).
+ *
+ * What the layer computes (sources are web pages about the DeepSeek-V3
+ * technical report; the tag in brackets is used in every comment below):
+ *   [digest-2.2]  "DeepSeek-V3技术报告" digest, mpbf.cn/news/71467, section 2.2
+ *                 "DeepSeekMoE 与无辅助损失": shared experts plus fine-grained
+ *                 routed experts; sigmoid affinities normalised over the K
+ *                 selected experts; top-K on affinity + bias with the gates
+ *                 taken from the raw affinities; after each step the bias of
+ *                 an overloaded expert drops by gamma and that of an
+ *                 underloaded one rises by gamma; each token uses at most M
+ *                 nodes, chosen by the summed affinities on each node; no
+ *                 token is dropped.
+ *   [digest-3.1]  same page, section 3.1 "FP8 混合精度": FP8 GEMM inputs with
+ *                 per-tile scale factors and higher-precision accumulation.
+ *   [digest-3.3]  same page, section 3.3: the all-to-all dispatch / combine
+ *                 that the on-device permutation and combine replace.
+ *   [resmic-moe]  "DeepSeek-V3架构深度解析", blog.resmic.cn/post/249.html,
+ *                 section "核心架构二": output = shared-expert sum + sum of
+ *                 gate-weighted routed experts; the router is a linear map.
+ *
+ * Notation: T tokens, d hidden width, E routed experts in G equal groups,
+ * K experts per token from at most M groups, I expert intermediate width,
+ * S shared experts. Expert FFN_e(v) = W2_e (silu(W1_e v) * (W3_e v)).
+ *
+ * Conventions for every call:
+ *   - All tensors are dense, row-major, and live in device memory unless a
+ *     parameter says "host". Every pointer must be 16-byte aligned.
+ *   - The caller owns all memory. The library allocates nothing on the device:
+ *     scratch space comes from `ws`, a device buffer of at least
+ *     moe_workspace_size() bytes, which must not be shared by two calls that
+ *     run at the same time. Its first 256 bytes must be zero before its first
+ *     use (they hold the device error word, see below).
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are reported synchronously, before any work is queued.
+ *     A launch failure returns MOE_ERR_CUDA.
+ *   - Kernels that wait on on-chip barriers give up after about a second,
+ *     write an error code into the first word of `ws` and return; the code is
+ *     read back with moe_device_error(). Out-of-range expert indices given to
+ *     moe_permute are skipped and reported the same way.
+ *   - T == 0 is a valid no-op.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad pointer, shape or combination */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid layer, but a shape this build does not run */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+  MOE_ERR_TIMEOUT = 4,      /* a device-side wait ran out (see moe_device_error) */
+  MOE_ERR_DEVICE = 5        /* device-side check failed (see moe_device_error) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+
+typedef struct {
+  int T, d, E, G, K, M, I, S;
+  int group_topk;     /* group score = sum of this many largest biased
+                         affinities in the group (2 in DeepSeek-V3 shapes) */
+  moe_dtype act;      /* x, out, router weights, yp: MOE_F32 or MOE_BF16 */
+  moe_dtype expert;   /* expert GEMM operands: == act, or MOE_E4M3 with act
+                         MOE_BF16 (1x128 activation tiles, 128x128 weight
+                         blocks, fp32 accumulation [digest-3.1]) */
+} moe_config;
+
+/* Expert weights. Element type is cfg->expert (router: cfg->act).
+ * w13 holds W1 (rows 0..I-1, the gate projection) above W3 (rows I..2I-1,
+ * the up projection) for each expert. For MOE_E4M3 each weight matrix carries
+ * one fp32 scale per 128x128 block: w = code * scale. */
+typedef struct {
+  const void* w_router;      /* [E, d]   act dtype                  */
+  const void* w13;           /* [E, 2I, d]                          */
+  const void* w2;            /* [E, d, I]                           */
+  const void* ws13;          /* [S, 2I, d]  shared experts          */
+  const void* ws2;           /* [S, d, I]                           */
+  const float* w13_scale;    /* E4M3: [E, 2I/128, d/128], else NULL */
+  const float* w2_scale;     /* E4M3: [E, d/128, I/128]             */
+  const float* ws13_scale;   /* E4M3: [S, 2I/128, d/128]            */
+  const float* ws2_scale;    /* E4M3: [S, d/128, I/128]             */
+} moe_weights;
+
+/* Bytes of device workspace that every call below needs for `cfg`
+ * (moe_layer_forward needs the most; one buffer of this size serves all).
+ * Limits checked here and by every call: E <= 512 with E % G == 0, G <= 32,
+ * 1 <= group_topk <= E/G, K <= 32, K <= M * (E/G), M <= G; for act BF16
+ * d % 128 == 0, I % 128 == 0 and E <= 256. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Router and routing [digest-2.2], [resmic-moe].
+ *   scores s = sigmoid(x W_r^T) [T, E] fp32, computed from x [T, d] and
+ *   w_router [E, d] unless scores_in (a [T, E] fp32 array) is given, in which
+ *   case x and w_router are ignored and s = scores_in.
+ *   s' = s + bias (fp32). Group score = sum of the group_topk largest s' of
+ *   the group; the M best groups are kept (ties: lower group index); the K
+ *   largest s' among their experts are chosen (ties: lower expert index) and
+ *   written to topk_idx [T, K] int32 in (s' desc, index asc) order.
+ *   topk_gate [T, K] fp32 = s_e / (sum of s over the K chosen experts).
+ *   counts [E] int32 = number of (token, slot) pairs per expert; it is zeroed
+ *   by this call. scores_out (nullable, [T, E] fp32) receives s.
+ *   bias [E] fp32 is read only. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
+                     const float* scores_in, const float* bias, float* scores_out,
+                     int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                     void* ws, moe_stream_t stream);
+
+/* Expert-major permutation (the on-device stand-in for the all-to-all
+ * dispatch [digest-3.3]; every pair is kept, no token is dropped).
+ *   counts [E] must be the histogram of topk_idx (as moe_route writes it).
+ *   offsets [E+1] = exclusive scan of counts (offsets[E] = T*K).
+ *   Position p in [offsets[e], offsets[e+1]) holds the tokens that chose
+ *   expert e, in ascending token order: sorted_tok [T*K] gives the token at p,
+ *   slot_pos [T, K] gives the position of slot k of token t.
+ *   xp [T*K, d] receives the gathered rows x[sorted_tok[p]] in cfg->act, or
+ *   for MOE_E4M3 the e4m3 codes of the 1x128 tiles of those rows with their
+ *   scales in xp_scale, laid out [d/128, T*K] (tile-major); xp_scale is NULL
+ *   otherwise. */
+moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* sorted_tok, int32_t* slot_pos,
+                       const void* x, void* xp, float* xp_scale,
+                       void* ws, moe_stream_t stream);
+
+/* Routed experts on the permuted rows [digest-2.2]:
+ *   yp[p] = FFN_e(xp[p]) for every p in [offsets[e], offsets[e+1]),
+ *   yp [T*K, d] in cfg->act, not yet scaled by the gates. offsets is read on
+ *   the device, so no host synchronisation is needed after moe_permute. */
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const float* xp_scale,
+                           const int32_t* offsets, const moe_weights* w, void* yp,
+                           void* ws, moe_stream_t stream);
+
+/* Shared experts and gate-weighted combine [resmic-moe]:
+ *   out[t] = sum_s FFN_s(x[t]) + sum_k topk_gate[t,k] * yp[slot_pos[t,k]]
+ *   out [T, d] in cfg->act. The routed sum is added in the epilogue of the
+ *   shared experts' down projection. x [T, d] in cfg->act. */
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot_pos,
+                       const float* topk_gate, const void* x, const moe_weights* w,
+                       void* out, void* ws, moe_stream_t stream);
+
+/* Auxiliary-loss-free bias update [digest-2.2], in place on bias [E] fp32:
+ *   counts_e * E >  T*K  ->  bias_e -= gamma   (overloaded)
+ *   counts_e * E <  T*K  ->  bias_e += gamma   (underloaded)
+ *   otherwise unchanged. The comparison is exact (integers); the add is fp32.
+ *   max_over_mean (nullable, device, 1 float) = max_e counts_e * E / (T*K). */
+moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float gamma,
+                           float* bias, float* max_over_mean, moe_stream_t stream);
+
+/* The whole layer: route, permute, routed experts, shared experts with the
+ * fused combine, and (when gamma != 0) the bias update, queued on `stream`.
+ * out [T, d] in cfg->act; topk_idx, topk_gate, counts as in moe_route;
+ * bias [E] fp32 is updated in place after routing when gamma != 0;
+ * max_over_mean as in moe_bias_update (nullable). */
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                             float* bias, float gamma, void* out, int32_t* topk_idx,
+                             float* topk_gate, int32_t* counts, float* max_over_mean,
+                             void* ws, moe_stream_t stream);
+
+/* 128x128 block quantisation of n_mat bf16 matrices [n_mat, rows, cols] to
+ * e4m3 codes q (same shape, 1 byte each) and fp32 scales
+ * [n_mat, ceil(rows/128), ceil(cols/128)]: scale = amax / 448 (1 if the block
+ * is all zero), code = e4m3(w / scale) rounded to nearest even and saturated
+ * to +/-448 [digest-3.1]. Used to prepare MOE_E4M3 expert weights. */
+moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols,
+                                     uint8_t* q, float* scale, moe_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device error word in `ws`.
+ * *code receives 0 when no device-side check has fired since the last call;
+ * the return value is MOE_ERR_TIMEOUT / MOE_ERR_DEVICE when one has. */
+moe_status moe_device_error(void* ws, moe_stream_t stream, int* code);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,46 @@
+// Shared definitions of the CUDA side of the MoE layer library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Device error word codes (first int of the workspace).
+enum DevErr : int {
+  kDevOk = 0,
+  kDevTimeoutProducer = 0x101,   // TMA producer gave up waiting for a free stage
+  kDevTimeoutMma = 0x102,        // MMA issuer gave up waiting for data / TMEM
+  kDevTimeoutEpilogue = 0x103,   // epilogue gave up waiting for an accumulator
+  kDevTimeoutDrain = 0x104,      // exit-time wait for in-flight copies ran out
+  kDevBadExpertIndex = 0x201,    // topk_idx entry outside [0, E)
+  kDevCountMismatch = 0x202,     // counts[] is not the histogram of topk_idx
+};
+
+// A device-side wait that sees no progress for this long gives up.
+constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;  // 1 s
+
+struct __align__(16) bf16x8 {
+  __nv_bfloat162 v[4];
+};
+
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ int read_error(const int* err) {
+  return err ? *reinterpret_cast<const volatile int*>(err) : 0;
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// e4m3 code of v (round to nearest even, saturating to +/-448).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+}  // namespace moe

@@ -1,0 +1,67 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for
+// sm_103a, bf16 operands, fp32 accumulation in tensor memory.
+//
+// C[row, n] = sum_k A[row, k] * B_g[n, k] for every row of group g. Both
+// operands are K-major and are moved global -> shared by TMA with 128-byte
+// swizzle. Work is split into 128 x BN output tiles; one CTA per SM walks the
+// tile list with a static stride. Warp roles inside a CTA (192 threads):
+//   warp 0      TMA producer (one lane): fills a STAGES-deep ring of A/B tiles
+//   warp 1      MMA issuer (one lane): tcgen05.mma into one of two TMEM
+//               accumulators, tcgen05.commit frees ring slots / signals tiles
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused math,
+//               stores to global memory
+// Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
+// the main loop of tile i+1.
+//
+// A launch covers up to two segments that share the epilogue:
+//   segment 0: `groups0` groups with device-side row offsets (routed experts
+//              on the expert-major permuted rows; the group sizes are read on
+//              the device, so no host synchronisation is needed);
+//   segment 1: one group of `rows1` rows (shared experts or the router).
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+enum class Epi : int {
+  kRouterSigmoid = 0,  // out fp32 [rows, n_valid] = sigmoid(acc)
+  kSwiGLU = 1,         // out bf16 [rows, ldo] = silu(gate) * up  (128 cols per tile)
+  kStore = 2,          // out bf16 [rows, ldo] = acc
+  kCombine = 3,        // out bf16 [T, ldo] = acc + sum_k gate * yp[slot_pos]
+};
+
+struct TcGemmParams {
+  int groups0;          // segment 0 groups (0: no segment 0)
+  const int* offsets0;  // [groups0 + 1] device row offsets of segment 0
+  int rows1;            // rows of segment 1 (0: no segment 1)
+  int n_tiles0, n_tiles1;
+  int k_blocks0, k_blocks1;  // K / 64 per segment
+  int I;                // expert intermediate width (B row / K addressing)
+  void* out0;
+  void* out1;
+  int ldo0, ldo1;       // output row strides (elements)
+  int n_valid;          // router: number of experts (output columns)
+  // kCombine
+  const int* slot_pos;  // [T, topk]
+  const float* gate;    // [T, topk]
+  const __nv_bfloat16* yp;  // [T*topk, ldo1]
+  int topk;
+  int* err;             // device error word
+};
+
+struct TcGemmLaunch {
+  Epi epi;
+  int bn;
+  CUtensorMap a0, b0, a1, b1;
+  TcGemmParams p;
+  int grid;
+  cudaStream_t stream;
+};
+
+// Queues one launch; returns the launch status.
+cudaError_t launch_tc_gemm(const TcGemmLaunch& L);
+
+}  // namespace moe

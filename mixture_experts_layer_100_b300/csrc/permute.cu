@@ -1,0 +1,242 @@
+// Expert-major permutation of the (token, slot) pairs and the row gather:
+// the single-GPU stand-in for the all-to-all dispatch of the DeepSeek-V3
+// pages ("DeepSeek-V3技术报告" digest, mpbf.cn, section 3.3). Every pair keeps
+// its place (no dropping, section 2.2); positions are expert-major and, inside
+// an expert, token-ascending.
+//
+// Three passes, no host synchronisation and no atomics on positions:
+//   rank    one warp per chunk of 32 tokens: per-chunk histogram and, for
+//           every pair, its rank among the earlier pairs of the chunk with
+//           the same expert (__match_any_sync over the pairs in order);
+//   scan    one warp per expert: exclusive scan of that expert's chunk
+//           histogram, offset by the expert's start (a sum over counts[]);
+//   scatter one warp per token: position = base[e][chunk] + rank; writes
+//           slot_pos / sorted_tok and copies the token row to its K places
+//           with 16-byte vector accesses (optionally quantising it to e4m3).
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 32;  // tokens per rank chunk (one warp)
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+    permute_rank_kernel(const int* __restrict__ topk_idx, int T, int K, int E, int nchunks,
+                        int* __restrict__ local_rank, int* __restrict__ chunk_hist, int* err) {
+  extern __shared__ int hist_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* hist = hist_all + warp * E;
+  const int c = blockIdx.x * kWarps + warp;
+  for (int e = lane; e < E; e += 32) hist[e] = 0;
+  __syncwarp();
+  if (c < nchunks) {
+    const int t0 = c * kChunk;
+    const int ntok = min(kChunk, T - t0);
+    const int npairs = ntok * K;
+    const int* src = topk_idx + (size_t)t0 * K;
+    int* dst = local_rank + (size_t)t0 * K;
+    for (int base = 0; base < npairs; base += 32) {
+      const int q = base + lane;
+      int e = q < npairs ? src[q] : -1;
+      if (e >= E || e < -1 || (q < npairs && e < 0)) {
+        set_error(err, kDevBadExpertIndex);
+        e = -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int before = __popc(peers & ((1u << lane) - 1u));
+      int r = 0;
+      if (e >= 0) r = hist[e] + before;
+      __syncwarp();
+      if (e >= 0 && before == 0) hist[e] += __popc(peers);
+      __syncwarp();
+      if (q < npairs) dst[q] = r;
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) chunk_hist[(size_t)e * nchunks + c] = hist[e];
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    permute_scan_kernel(const int* __restrict__ counts, const int* __restrict__ chunk_hist, int E, int nchunks,
+                        int* __restrict__ chunk_base, int* __restrict__ offsets, int* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kWarps + warp;
+  if (e >= E) return;
+  int start = 0;
+  for (int j = lane; j < e; j += 32) start += counts[j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) start += __shfl_xor_sync(0xffffffffu, start, o);
+  const int* h = chunk_hist + (size_t)e * nchunks;
+  int* out = chunk_base + (size_t)e * nchunks;
+  int carry = start;
+  for (int c0 = 0; c0 < nchunks; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < nchunks ? h[c] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (c < nchunks) out[c] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    if (carry - start != counts[e]) set_error(err, kDevCountMismatch);
+    offsets[e] = start;
+    if (e == E - 1) offsets[E] = start + counts[e];
+  }
+}
+
+template <typename VecT>
+__global__ void __launch_bounds__(kWarps * 32)
+    permute_scatter_kernel(const int* __restrict__ topk_idx, const int* __restrict__ local_rank,
+                           const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
+                           const VecT* __restrict__ x, int row_vecs, int* __restrict__ sorted_tok,
+                           int* __restrict__ slot_pos, VecT* __restrict__ xp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    int pos = 0;
+    if (lane < K) {
+      const int e = topk_idx[(size_t)t * K + lane];
+      if (e >= 0 && e < E) {
+        pos = chunk_base[(size_t)e * nchunks + t / kChunk] + local_rank[(size_t)t * K + lane];
+        slot_pos[(size_t)t * K + lane] = pos;
+        sorted_tok[pos] = t;
+      } else {
+        pos = -1;
+      }
+    }
+    const VecT* src = x + (size_t)t * row_vecs;
+    for (int i = lane; i < row_vecs; i += 32) {
+      const VecT val = src[i];
+      for (int k = 0; k < K; ++k) {
+        const int pk = __shfl_sync(0xffffffffu, pos, k);
+        if (pk >= 0) xp[(size_t)pk * row_vecs + i] = val;
+      }
+    }
+  }
+}
+
+// Same positions; each token row (bf16) is cut into 1x128 tiles and written
+// to its K places as e4m3 codes, with one fp32 scale per tile:
+// scale = amax / 448 (1 for an all-zero tile), code = e4m3(v / scale).
+// A half-warp covers one 128-element tile (8 elements per lane). When xq is
+// given, the quantised row is also written once in token order (for the
+// shared experts). Scales are stored tile-major: scale[tile * rows + row].
+__global__ void __launch_bounds__(kWarps * 32)
+    permute_scatter_e4m3_kernel(const int* __restrict__ topk_idx, const int* __restrict__ local_rank,
+                                const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
+                                const __nv_bfloat16* __restrict__ x, int d, int* __restrict__ sorted_tok,
+                                int* __restrict__ slot_pos, uint8_t* __restrict__ xp, float* __restrict__ xp_scale,
+                                uint8_t* __restrict__ xq, float* __restrict__ xq_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = d / 128;
+  const int TK = T * K;
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    int pos = -1;
+    if (lane < K) {
+      const int e = topk_idx[(size_t)t * K + lane];
+      if (e >= 0 && e < E) {
+        pos = chunk_base[(size_t)e * nchunks + t / kChunk] + local_rank[(size_t)t * K + lane];
+        slot_pos[(size_t)t * K + lane] = pos;
+        sorted_tok[pos] = t;
+      }
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    // two tiles per warp iteration: lanes 0..15 tile 2i, lanes 16..31 tile 2i+1
+    for (int tile0 = 0; tile0 < ntiles; tile0 += 2) {
+      const int tile = tile0 + (lane >> 4);
+      const bool act = tile < ntiles;
+      float f[8];
+      float amax = 0.0f;
+      if (act) {
+        const uint4 w = src[tile * 16 + (lane & 15)];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 v = __bfloat1622float2(h[j]);
+          f[2 * j] = v.x;
+          f[2 * j + 1] = v.y;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      uint2 packed = make_uint2(0, 0);
+      if (act) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], scale)) << (8 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], scale)) << (8 * j);
+        packed = make_uint2(lo, hi);
+      }
+      for (int k = 0; k < K; ++k) {
+        const int pk = __shfl_sync(0xffffffffu, pos, k);
+        if (act && pk >= 0) {
+          reinterpret_cast<uint2*>(xp + (size_t)pk * d + tile * 128)[lane & 15] = packed;
+          if ((lane & 15) == 0) xp_scale[(size_t)tile * TK + pk] = scale;
+        }
+      }
+      if (act && xq != nullptr) {
+        reinterpret_cast<uint2*>(xq + (size_t)t * d + tile * 128)[lane & 15] = packed;
+        if ((lane & 15) == 0) xq_scale[(size_t)tile * T + t] = scale;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int permute_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+
+cudaError_t launch_permute_rank(const int* topk_idx, int T, int K, int E, int* local_rank, int* chunk_hist, int* err,
+                                cudaStream_t st) {
+  const int nchunks = permute_chunks(T);
+  const int blocks = (nchunks + kWarps - 1) / kWarps;
+  permute_rank_kernel<<<blocks, kWarps * 32, (size_t)kWarps * E * sizeof(int), st>>>(topk_idx, T, K, E, nchunks,
+                                                                                      local_rank, chunk_hist, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scan(const int* counts, const int* chunk_hist, int T, int E, int* chunk_base, int* offsets,
+                                int* err, cudaStream_t st) {
+  const int nchunks = permute_chunks(T);
+  permute_scan_kernel<<<(E + kWarps - 1) / kWarps, kWarps * 32, 0, st>>>(counts, chunk_hist, E, nchunks, chunk_base,
+                                                                         offsets, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, const int* chunk_base, int T, int K,
+                                   int E, const void* x, size_t row_bytes, int* sorted_tok, int* slot_pos, void* xp,
+                                   int num_sms, cudaStream_t st) {
+  const int nchunks = permute_chunks(T);
+  const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
+  if (row_bytes % 16 == 0) {
+    permute_scatter_kernel<uint4><<<blocks, kWarps * 32, 0, st>>>(
+        topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint4*>(x), (int)(row_bytes / 16),
+        sorted_tok, slot_pos, static_cast<uint4*>(xp));
+  } else {
+    permute_scatter_kernel<uint32_t><<<blocks, kWarps * 32, 0, st>>>(
+        topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint32_t*>(x), (int)(row_bytes / 4),
+        sorted_tok, slot_pos, static_cast<uint32_t*>(xp));
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
+                                        int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
+                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, int num_sms,
+                                        cudaStream_t st) {
+  const int nchunks = permute_chunks(T);
+  const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
+  permute_scatter_e4m3_kernel<<<blocks, kWarps * 32, 0, st>>>(topk_idx, local_rank, chunk_base, T, K, E, nchunks, x,
+                                                              d, sorted_tok, slot_pos, xp, xp_scale, xq, xq_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

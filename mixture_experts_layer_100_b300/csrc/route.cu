@@ -1,0 +1,217 @@
+// Routing: group-limited top-K on sigmoid affinity + bias, gates from the raw
+// affinities, and the per-expert load count ("DeepSeek-V3技术报告" digest,
+// mpbf.cn, section 2.2).
+//
+// One warp per token. Expert e lives in lane e % 32, register e / 32. The
+// selection compares 64-bit keys (order-preserving bits of s' << 32 | ~e), so
+// a plain maximum picks the largest biased affinity and, among equal values,
+// the lowest expert index.
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ uint64_t score_key(float v, int e) {
+  if (v == 0.0f) v = 0.0f;  // -0 and +0 compare equal: give them one key
+  uint32_t b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)b << 32) | (uint32_t)(~(uint32_t)e);
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, k, o);
+    k = other > k ? other : k;
+  }
+  return k;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kWarps * 32)
+    route_select_kernel(const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int G,
+                        int K, int M, int gk, int* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                        int* __restrict__ counts) {
+  extern __shared__ float sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* hist = reinterpret_cast<int*>(sh);           // [E]
+  float* sp_all = sh + E;                           // [kWarps][E]
+  float* sp = sp_all + warp * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+
+  const int gsz = E / G;
+  float b[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    b[j] = e < E ? bias[e] : 0.0f;
+  }
+
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    const float* srow = scores + (size_t)t * E;
+    float s[NPL], v[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      s[j] = e < E ? srow[e] : 0.0f;
+      v[j] = __fadd_rn(s[j], b[j]);  // s' = s + b, one fp32 add
+      if (e < E) sp[e] = v[j];
+    }
+    __syncwarp();
+
+    // group score: sum of the gk largest s' of the group, largest first
+    float gs = -INFINITY;
+    if (lane < G) {
+      float top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int j = 0; j < gsz; ++j) {
+        float x = sp[lane * gsz + j];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (r < gk && x > top[r]) {
+            const float tmp = top[r];
+            top[r] = x;
+            x = tmp;
+          }
+        }
+      }
+      gs = top[0];
+      for (int r = 1; r < gk; ++r) gs = __fadd_rn(gs, top[r]);
+    }
+    // the M best groups (ties: lower group index)
+    int rank = 0;
+    for (int g2 = 0; g2 < G; ++g2) {
+      const float o = __shfl_sync(0xffffffffu, gs, g2);
+      rank += (o > gs) || (o == gs && g2 < lane);
+    }
+    const unsigned gmask = __ballot_sync(0xffffffffu, lane < G && rank < M);
+
+    uint64_t key[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (e < E && ((gmask >> (e / gsz)) & 1u)) ? score_key(v[j], e) : 0ull;
+    }
+    // K rounds of warp arg-max
+    int my_e = -1;
+    float my_s = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      uint64_t best = key[0];
+#pragma unroll
+      for (int j = 1; j < NPL; ++j) best = key[j] > best ? key[j] : best;
+      best = warp_max_u64(best);
+      const int e = (int)(~(uint32_t)best);
+      const int owner = e & 31, slot = e >> 5;
+      float se = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) {
+        if (lane == owner && j == slot) {
+          key[j] = 0ull;
+          se = s[j];
+        }
+      }
+      se = __shfl_sync(0xffffffffu, se, owner);
+      if (lane == k) {
+        my_e = e;
+        my_s = se;
+      }
+    }
+    // gates: raw affinity over the sum of the K chosen raw affinities
+    float sum = 0.0f;
+    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_s, k));
+    if (lane < K) {
+      topk_idx[(size_t)t * K + lane] = my_e;
+      topk_gate[(size_t)t * K + lane] = __fdiv_rn(my_s, sum);
+      atomicAdd(&hist[my_e], 1);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = hist[e];
+    if (c) atomicAdd(&counts[e], c);
+  }
+}
+
+// Router for fp32 activations: s = sigmoid(x W_r^T), plain FMA tiles
+// (64 tokens x 32 experts per block, K staged through shared memory).
+__global__ void __launch_bounds__(256) router_f32_kernel(const float* __restrict__ x, const float* __restrict__ wr,
+                                                         int T, int d, int E, float* __restrict__ scores) {
+  __shared__ float xs[64][33];
+  __shared__ float ws[32][33];
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int k0 = 0; k0 < d; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int r = i / 32, c = i % 32;
+      xs[r][c] = (t0 + r < T && k0 + c < d) ? x[(size_t)(t0 + r) * d + k0 + c] : 0.0f;
+    }
+    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
+      const int r = i / 32, c = i % 32;
+      ws[r][c] = (e0 + r < E && k0 + c < d) ? wr[(size_t)(e0 + r) * d + k0 + c] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float w = ws[tx][k];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(xs[ty + 8 * i][k], w, acc[i]);
+    }
+    __syncthreads();
+  }
+  const int e = e0 + tx;
+  if (e < E) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + ty + 8 * i;
+      if (t < T) scores[(size_t)t * E + e] = 1.0f / (1.0f + expf(-acc[i]));
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_select(const float* scores, const float* bias, int T, int E, int G, int K, int M, int gk,
+                                int* topk_idx, float* topk_gate, int* counts, int num_sms, cudaStream_t st) {
+  const int npl = (E + 31) / 32;
+  const size_t smem = (size_t)(E + kWarps * E) * sizeof(float);
+  const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 4));
+#define MOE_ROUTE_CASE(N)                                                                         \
+  case N:                                                                                         \
+    route_select_kernel<N><<<blocks, kWarps * 32, smem, st>>>(scores, bias, T, E, G, K, M, gk,    \
+                                                              topk_idx, topk_gate, counts);       \
+    break;
+  switch (npl) {
+    MOE_ROUTE_CASE(1)
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(3)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(5)
+    MOE_ROUTE_CASE(6)
+    MOE_ROUTE_CASE(7)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(12)
+    MOE_ROUTE_CASE(16)
+    default:
+      if (npl <= 12) {
+        route_select_kernel<12><<<blocks, kWarps * 32, smem, st>>>(scores, bias, T, E, G, K, M, gk, topk_idx,
+                                                                   topk_gate, counts);
+      } else {
+        route_select_kernel<16><<<blocks, kWarps * 32, smem, st>>>(scores, bias, T, E, G, K, M, gk, topk_idx,
+                                                                   topk_gate, counts);
+      }
+  }
+#undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_f32(const float* x, const float* wr, int T, int d, int E, float* scores, cudaStream_t st) {
+  dim3 grid((T + 63) / 64, (E + 31) / 32);
+  router_f32_kernel<<<grid, 256, 0, st>>>(x, wr, T, d, E, scores);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -25,3 +25,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionstart(session):
+    """Build the CUDA library in-tree if a source is newer than the .so."""
+    from mixture_experts_layer_100_b300 import build
+
+    if build.needs_build():
+        build.build()

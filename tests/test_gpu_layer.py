@@ -1,0 +1,230 @@
+"""GPU parity of the whole layer (moe_layer_forward) and of the individual
+entry points, against the oracle on the same seeded inputs.
+
+Small shapes are compared element by element on every token; they span
+several 128-row tiles per expert, ragged tails, both down-projection tile
+widths, S = 0 / 1 / 2 shared experts and the degenerate cases (one token,
+all-tied router, zero routed weights, all tokens on a few experts, T = 0).
+The full-size presets are compared on seeded token samples.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_100_b300 import synth
+from oracle import moe_oracle as om
+from tests.layer_helpers import DEV, compare, device_weights, oracle_rows, run_layer
+
+pytestmark = pytest.mark.gpu
+
+BASE = synth.PRESETS["mid_t4096_d2048_e64_bf16"]
+
+SMALL = {
+    "t300_d256_e16_i256": dict(T=300, d=256, E=16, G=4, K=4, M=2, I=256, S=1),
+    "t515_d384_e32_i384_s2": dict(T=515, d=384, E=32, G=8, K=6, M=3, I=384, S=2),
+    "t1_d256_e16": dict(T=1, d=256, E=16, G=4, K=4, M=2, I=128, S=1),
+    "t700_d128_e256_k8": dict(T=700, d=128, E=256, G=8, K=8, M=4, I=128, S=1),
+    "t129_d512_e64_s0": dict(T=129, d=512, E=64, G=8, K=6, M=3, I=256, S=0),
+}
+
+
+def small_preset(name, **over):
+    kw = dict(SMALL[name])
+    kw.update(over)
+    return BASE.replace(name=name, zipf=False, bias="u0.01", **kw)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_layer_bf16_all_tokens(name):
+    p = small_preset(name)
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    ref = oracle_rows(p, w, x, b)
+    compare(p, res, ref, b)
+    np.testing.assert_array_equal(res["counts"].cpu().numpy(),
+                                  om.expert_counts(res["topk_idx"].cpu().numpy(), p.E))
+
+
+def test_tiny_fp32_preset_with_bias_steps():
+    """The fp32 preset: full output parity at 1e-5, then its 10 forward +
+    bias-update steps; the bias trajectory must equal the oracle's."""
+    p = synth.PRESETS["tiny_t256_d512_e16_fp32"]
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    wd = device_weights(w)
+    xd, bd = x.to(DEV), b.clone().to(DEV)
+    b_ref = b.numpy().copy()
+    ws = None
+    for step in range(p.steps):
+        res = run_layer(p, wd, xd, bd, gamma=p.gamma, ws=ws)
+        ws = res["ws"]
+        ref = oracle_rows(p, w, x, torch.from_numpy(b_ref))
+        compare(p, res, ref, b_ref, max_flip=0.0)
+        b_ref = om.bias_update(om.expert_counts(ref["topk_idx"], p.E), b_ref, p.gamma, p.T, p.K)
+        np.testing.assert_array_equal(bd.cpu().numpy(), b_ref)
+
+
+def test_all_tokens_on_four_experts():
+    """Bias +1 on group 0: every token takes its four experts (4 x T rows)."""
+    p = small_preset("t300_d256_e16_i256", T=1000)
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = torch.zeros(p.E)
+    b[:4] = 1.0
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    c = res["counts"].cpu().numpy()
+    assert list(c[:4]) == [p.T] * 4 and c[4:].sum() == 0
+    compare(p, res, oracle_rows(p, w, x, b), b)
+
+
+def test_zero_router_all_ties():
+    p = small_preset("t300_d256_e16_i256")
+    w = synth.make_weights(p)
+    w.w_router.zero_()
+    x = synth.make_x(p, w.w_router)
+    b = torch.zeros(p.E)
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    idx = res["topk_idx"].cpu().numpy()
+    assert (idx == np.arange(4)[None, :]).all()
+    assert (res["topk_gate"].cpu().numpy() == np.float32(0.25)).all()
+    compare(p, res, oracle_rows(p, w, x, b), b)
+
+
+def test_zero_routed_weights_give_shared_only():
+    p = small_preset("t515_d384_e32_i384_s2")
+    w = synth.make_weights(p, zero_routed=True)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    shared = om.shared_output(x.double().numpy(), w.ws13.double().numpy(), w.ws2.double().numpy())
+    got = res["out"].float().cpu().numpy()
+    assert np.abs(got - shared).max() / np.abs(shared).max() <= 2e-2
+
+
+def test_empty_batch_is_a_no_op():
+    from mixture_experts_layer_100_b300 import binding as B
+    p = small_preset("t300_d256_e16_i256", T=0)
+    w = synth.make_weights(p.replace(T=1))
+    cfg = B.config_from_preset(p)
+    ws = B.alloc_workspace(cfg)
+    b = torch.zeros(p.E, device=DEV)
+    counts = torch.full((p.E,), 5, dtype=torch.int32, device=DEV)
+    dummy = torch.empty(16, dtype=torch.int32, device=DEV)
+    B.moe_layer_forward(cfg, None, B.make_weights(**device_weights(w)), b, 1e-3, None, dummy, dummy.float(),
+                        counts, None, ws)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0 and b.abs().sum().item() == 0
+
+
+def test_entry_points_compose_to_the_layer():
+    """route -> permute -> grouped_ffn -> combine -> bias_update gives the
+    same bits as moe_layer_forward."""
+    from mixture_experts_layer_100_b300 import binding as B
+    p = small_preset("t515_d384_e32_i384_s2")
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router).to(DEV)
+    b0 = synth.make_bias(p).to(DEV)
+    wd = device_weights(w)
+    bl = b0.clone()
+    res = run_layer(p, wd, x, bl, gamma=p.gamma)
+    cfg = B.config_from_preset(p)
+    ws = B.alloc_workspace(cfg)
+    T, K, E, d = p.T, p.K, p.E, p.d
+    idx = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    gate = torch.empty(T, K, dtype=torch.float32, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    scores = torch.empty(T, E, dtype=torch.float32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    st = torch.empty(T * K, dtype=torch.int32, device=DEV)
+    sp = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    xp = torch.empty(T * K, d, dtype=torch.bfloat16, device=DEV)
+    yp = torch.empty(T * K, d, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
+    weights = B.make_weights(**wd)
+    bs = b0.clone()
+    B.moe_route(cfg, x, wd["w_router"], None, bs, scores, idx, gate, counts, ws)
+    B.moe_permute(cfg, idx, counts, off, st, sp, x, xp, None, ws)
+    B.moe_grouped_ffn(cfg, xp, None, off, weights, yp, ws)
+    B.moe_combine(cfg, yp, sp, gate, x, weights, out, ws)
+    B.moe_bias_update(cfg, counts, p.gamma, bs)
+    torch.cuda.synchronize()
+    assert B.moe_device_error(ws) == 0
+    assert torch.equal(idx, res["topk_idx"]) and torch.equal(counts, res["counts"])
+    assert torch.equal(out, res["out"])
+    assert torch.equal(bs, bl)
+    # the router scores: sigmoid(x W_r^T) to fp32 rounding of the bf16 GEMM
+    s_ref = om.router_scores(x.float().cpu().numpy(), w.w_router.float().numpy())
+    assert np.abs(scores.cpu().numpy() - s_ref).max() < 2e-6
+    # and the routed rows themselves: yp[p] = FFN_e(x[sorted_tok[p]])
+    o = off.cpu().numpy()
+    for e in [0, 7, E - 1]:
+        rows = np.arange(o[e], o[e + 1])[:5]
+        if len(rows) == 0:
+            continue
+        toks = st.cpu().numpy()[rows]
+        ref = om.swiglu_ffn(x.float().cpu().numpy()[toks], w.w13[e].double().numpy(), w.w2[e].double().numpy())
+        got = yp[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+        assert np.abs(got - ref).max() / np.abs(ref).max() <= 2e-2
+
+
+def test_layer_is_deterministic():
+    p = small_preset("t515_d384_e32_i384_s2")
+    w = synth.make_weights(p)
+    wd = device_weights(w)
+    x = synth.make_x(p, w.w_router).to(DEV)
+    b = synth.make_bias(p).to(DEV)
+    r1 = run_layer(p, wd, x, b)
+    r2 = run_layer(p, wd, x, b)
+    assert torch.equal(r1["out"], r2["out"]) and torch.equal(r1["topk_idx"], r2["topk_idx"])
+
+
+def test_mid_preset_sampled_tokens():
+    p = synth.PRESETS["mid_t4096_d2048_e64_bf16"]
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    toks = np.sort(np.random.default_rng(0).choice(p.T, 768, replace=False))
+    toks = np.unique(np.concatenate([toks, [0, p.T - 1]]))
+    compare(p, res, oracle_rows(p, w, x, b, toks), b, tokens=toks)
+    assert res["counts"].sum().item() == p.T * p.K
+
+
+@pytest.fixture(scope="module")
+def v3_weights():
+    p = synth.PRESETS["v3_t16384_d7168_e256_bf16"]
+    w = synth.make_weights(p, device=DEV)
+    torch.cuda.synchronize()
+    yield w
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_v3_preset_sampled_tokens(v3_weights):
+    p = synth.PRESETS["v3_t16384_d7168_e256_bf16"]
+    w = v3_weights
+    x = synth.make_x(p, w.w_router, device=DEV)
+    b = synth.make_bias(p)
+    wd = device_weights(w)
+    res = run_layer(p, wd, x, b.to(DEV), gamma=p.gamma)
+    toks = np.unique(np.concatenate([np.random.default_rng(1).choice(p.T, 40, replace=False), [0, p.T - 1]]))
+    err, flips = compare(p, res, oracle_rows(p, w, x.cpu(), b, toks), b, tokens=toks, max_flip=0.05)
+    c = res["counts"].cpu().numpy()
+    assert c.sum() == p.T * p.K
+    assert res["max_over_mean"].item() == np.float32(c.max() * p.E / (p.T * p.K))
+    # skewed raw load: the hottest expert well above the mean
+    assert c.max() > 4 * c.mean()
+
+
+@pytest.mark.parametrize("name,sample", [("v3_decode_t64_bf16", None), ("v3_decode_t512_bf16", 48)])
+def test_v3_decode_presets(v3_weights, name, sample):
+    p = synth.PRESETS[name]
+    w = v3_weights
+    x = synth.make_x(p, w.w_router, device=DEV)
+    b = synth.make_bias(p)
+    res = run_layer(p, device_weights(w), x, b.to(DEV))
+    toks = None if sample is None else np.sort(np.random.default_rng(2).choice(p.T, sample, replace=False))
+    compare(p, res, oracle_rows(p, w, x.cpu(), b, toks), b, tokens=toks, max_flip=0.05)
