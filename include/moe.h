@@ -173,6 +173,15 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
 moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols,
                                      uint8_t* q, float* scale, moe_stream_t stream);
 
+/* Profiling hook. After this call, every moe_layer_forward made from the
+ * calling thread records events[i] (cudaEvent_t handles owned by the caller)
+ * on its stream at stage boundary i: 0 before the router, 1 after the router
+ * GEMM, 2 after the top-K selection, 3 after the permutation, 4 after the
+ * expert GEMM1 (SwiGLU, routed and shared experts in one launch), 5 after the
+ * routed down projection, 6 after the shared down projection with the fused
+ * combine, 7 after the bias update. count must be 0 (hook off) or >= 8. */
+moe_status moe_set_stage_events(void* const* events, int count);
+
 /* Synchronises `stream`, then reads and clears the device error word in `ws`.
  * *code receives 0 when no device-side check has fired since the last call;
  * the return value is MOE_ERR_TIMEOUT / MOE_ERR_DEVICE when one has. */

@@ -57,6 +57,7 @@ _SIGS = {
     "moe_layer_forward": [ctypes.POINTER(moe_config), _P, ctypes.POINTER(moe_weights), _P, ctypes.c_float,
                           _P, _P, _P, _P, _P, _P, _P],
     "moe_quantize_weights_e4m3": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
+    "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
     "moe_status_string": [ctypes.c_int],
 }
@@ -153,6 +154,15 @@ def moe_quantize_weights_e4m3(w, q, scale, stream=None):
     n_mat, rows, cols = w.shape
     _check("moe_quantize_weights_e4m3", lib.moe_quantize_weights_e4m3(
         _ptr(w), n_mat, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_set_stage_events(events) -> None:
+    """events: list of >= 8 recorded torch.cuda.Event (or None to switch off)."""
+    if not events:
+        _check("moe_set_stage_events", lib.moe_set_stage_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check("moe_set_stage_events", lib.moe_set_stage_events(arr, len(events)))
 
 
 def moe_device_error(ws, stream=None) -> int:

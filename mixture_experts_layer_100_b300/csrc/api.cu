@@ -427,6 +427,14 @@ moe_status check_weights(const moe_config& c, const moe_weights* w, bool routed,
 
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
+thread_local cudaEvent_t g_stage_events[8];
+thread_local bool g_stage_on = false;
+
+moe_status stage_mark(int i, cudaStream_t st) {
+  if (g_stage_on) MOE_CUDA(cudaEventRecord(g_stage_events[i], st));
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -519,8 +527,15 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
   if (c.T > 0 && (!ok_ptr(x) || !ok_ptr(out) || !ok_ptr(w->w_router))) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Layout Lw = layout(c);
-  MOE_TRY(route_stage(c, x, w->w_router, nullptr, bias, nullptr, topk_idx, topk_gate, counts, ws, st));
+  MOE_TRY(stage_mark(0, st));
+  MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
   if (c.T > 0) {
+    float* scores = at<float>(ws, Lw.scores);
+    MOE_TRY(router_scores(c, x, w->w_router, scores, ws, st));
+    MOE_TRY(stage_mark(1, st));
+    MOE_CUDA(launch_route_select(scores, bias, c.T, c.E, c.G, c.K, c.M, c.group_topk, topk_idx, topk_gate, counts,
+                                 num_sms(), st));
+    MOE_TRY(stage_mark(2, st));
     int32_t* offsets = at<int32_t>(ws, Lw.offsets);
     int32_t* slot_pos = at<int32_t>(ws, Lw.slot_pos);
     void* xp = at<void>(ws, Lw.xp);
@@ -529,12 +544,17 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
     MOE_TRY(permute_stage(c, topk_idx, counts, offsets, at<int32_t>(ws, Lw.sorted_tok), slot_pos, x, xp,
                           f8 ? at<float>(ws, Lw.xp_scale) : nullptr, f8 ? at<uint8_t>(ws, Lw.xq) : nullptr,
                           f8 ? at<float>(ws, Lw.xq_scale) : nullptr, ws, st));
+    MOE_TRY(stage_mark(3, st));
     MOE_TRY(gemm1_stage(c, xp, offsets, x, w, true, true, ws, st));
+    MOE_TRY(stage_mark(4, st));
     MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
+    MOE_TRY(stage_mark(5, st));
     MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));
+    MOE_TRY(stage_mark(6, st));
+    if (gamma != 0.0f)
+      MOE_CUDA(launch_bias_update(counts, c.E, (long long)c.T * c.K, gamma, bias, max_over_mean, st));
+    MOE_TRY(stage_mark(7, st));
   }
-  if (gamma != 0.0f && c.T > 0)
-    MOE_CUDA(launch_bias_update(counts, c.E, (long long)c.T * c.K, gamma, bias, max_over_mean, st));
   return MOE_OK;
 }
 
@@ -545,6 +565,20 @@ moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int col
   if (!ok_ptr(w) || !ok_ptr(q) || scale == nullptr) return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_quantize_blocks(static_cast<const __nv_bfloat16*>(w), n_mat, rows, cols, q, scale,
                                   reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_set_stage_events(void* const* events, int count) {
+  if (count == 0) {
+    g_stage_on = false;
+    return MOE_OK;
+  }
+  if (events == nullptr || count < 8) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 8; ++i) {
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_stage_on = true;
   return MOE_OK;
 }
 
