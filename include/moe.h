@@ -173,6 +173,36 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
 moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols,
                                      uint8_t* q, float* scale, moe_stream_t stream);
 
+/* Bytes of the fixed device array that moe_permute_static uses as scratch. */
+#define MOE_PERMUTE_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory: code that is handed only its input and output buffers by a host
+ * framework with no scratch hook (a plugin inside another engine, say), or
+ * that runs where device allocation after start-up is not allowed (a fixed
+ * memory budget set once at start). There is no counterpart on the pages; it
+ * is a packaging variant of moe_permute for such callers.
+ *   Same inputs and outputs as moe_permute for act == expert (row copies; no
+ *   e4m3 tiles). Scratch comes from one static device array of
+ *   MOE_PERMUTE_STATIC_SCRATCH_BYTES (4 MiB) that every GPU which loads the
+ *   library keeps until the process exits. A call needs
+ *   256 + 4*T*K + 8*E*ceil(T/32) bytes of it (each part rounded up to 256);
+ *   larger calls return MOE_ERR_UNSUPPORTED before any work is queued
+ *   (T = 16384, K = 8, E = 256 needs 1.5 MiB; T = 32768 needs 3 MiB).
+ *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *   library routine.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current) and keeps it; make that
+ *   first call before any stream capture.
+ *   All calls on a device share the one array and leave their contents in it;
+ *   each call clears the part that must start at zero. Calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race on the array
+ *   and must be serialised by the caller. Out-of-range expert indices are
+ *   skipped, but not reported (moe_device_error does not see this array). */
+moe_status moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_tok, int32_t* slot_pos,
+                              const void* x, void* xp, moe_stream_t stream);
+
 /* Profiling hook. After this call, every moe_layer_forward made from the
  * calling thread records events[i] (cudaEvent_t handles owned by the caller)
  * on its stream at stage boundary i: 0 before the router, 1 after the router

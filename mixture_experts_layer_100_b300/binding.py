@@ -57,6 +57,7 @@ _SIGS = {
     "moe_layer_forward": [ctypes.POINTER(moe_config), _P, ctypes.POINTER(moe_weights), _P, ctypes.c_float,
                           _P, _P, _P, _P, _P, _P, _P],
     "moe_quantize_weights_e4m3": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
+    "moe_permute_static": [ctypes.POINTER(moe_config)] + [_P] * 7 + [_P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
     "moe_status_string": [ctypes.c_int],
@@ -125,6 +126,12 @@ def moe_permute(cfg, topk_idx, counts, offsets, sorted_tok, slot_pos, x, xp, xp_
     _check("moe_permute", lib.moe_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
                                           _ptr(sorted_tok), _ptr(slot_pos), _ptr(x), _ptr(xp), _ptr(xp_scale),
                                           _ptr(ws), _stream(stream)))
+
+
+def moe_permute_static(cfg, topk_idx, counts, offsets, sorted_tok, slot_pos, x, xp, stream=None):
+    _check("moe_permute_static", lib.moe_permute_static(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts),
+                                                        _ptr(offsets), _ptr(sorted_tok), _ptr(slot_pos), _ptr(x),
+                                                        _ptr(xp), _stream(stream)))
 
 
 def moe_grouped_ffn(cfg, xp, xp_scale, offsets, weights: moe_weights, yp, ws, stream=None):
