@@ -37,7 +37,7 @@ METRIC = "MoE-layer tokens/sec (1×B300, V3 shape T=16K bf16); % tensor/HBM roof
 DEFAULT_PRESET = "v3_t16384_d7168_e256_bf16"
 STAGES = ["router_gemm", "route_select", "permute", "gemm1_swiglu", "gemm2_routed", "gemm2_shared_combine",
           "bias_update"]
-KERNELS_PER_STEP = 9  # router, select, rank, scan, scatter, gemm1, gemm2, gemm2+combine, bias
+KERNELS_PER_STEP = 10  # router, select, rank, scan, scatter, gemm1, gemm2, routed sum, gemm2+combine, bias
 
 
 def parse():
@@ -173,7 +173,8 @@ def hbm_bytes(p):
         "router_gemm": p.T * p.d * a + p.E * p.d * a + p.T * p.E * 4,
         "route_select": p.T * p.E * 4 + p.T * p.K * 8,
         "permute": p.T * p.d * a + p.T * p.K * p.d * a + p.T * p.K * 16,
-        "gemm2_shared_combine": p.T * p.K * p.d * a + p.T * p.d * a + p.T * p.K * 8,
+        # routed sum: K gathered rows in, r out; epilogue: r in, out written
+        "gemm2_shared_combine": p.T * p.K * p.d * a + 3 * p.T * p.d * a + p.T * p.K * 8,
     }
 
 

@@ -5,6 +5,7 @@
 
 #include <cstring>
 
+#include "gemm_fp8.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
 #include "moe.h"
@@ -92,6 +93,7 @@ moe_status check_config(const moe_config* c) {
   if (c->act == MOE_BF16) {
     if (c->d % 128 != 0 || c->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->E > 256) return MOE_ERR_UNSUPPORTED;
+    if (c->expert == MOE_E4M3 && c->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   } else if (c->d % 4 != 0) {
     return MOE_ERR_UNSUPPORTED;
   }
@@ -234,9 +236,110 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
   return MOE_OK;
 }
 
+// ---- FP8 expert GEMMs (e4m3 tiles, fp32 promotion per 128-wide K block)
+moe_status fp8_gemm1(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
+                     const uint8_t* xq, const float* xq_scale, const moe_weights* w, bool routed, bool shared,
+                     void* ws, cudaStream_t st) {
+  const Layout Lw = layout(c);
+  const int TK = c.T * c.K;
+  Fp8GemmLaunch L{};
+  L.epi = Fp8Epi::kSwiGLU;
+  long long tiles = 0;
+  if (routed) {
+    MOE_TRY(map_2d(&L.a0, xp, 1, c.d, TK, 128, 128));
+    MOE_TRY(map_3d(&L.b0, w->w13, 1, c.d, 2 * (uint64_t)c.I, c.E, 128, 64));
+    L.p.groups0 = c.E;
+    L.p.offsets0 = offsets;
+    L.p.rows_total0 = TK;
+    L.p.n_tiles0 = c.I / 128;
+    L.p.k_blocks0 = c.d / 128;
+    L.p.a_scale0 = xp_scale;
+    L.p.b_scale0 = w->w13_scale;
+    L.p.out0 = at<void>(ws, Lw.h);
+    L.p.out_scale0 = at<float>(ws, Lw.h_scale);
+    L.p.ldo0 = c.I;
+    tiles += ((long long)TK / 128 + c.E) * L.p.n_tiles0;
+  }
+  if (shared && c.S > 0) {
+    MOE_TRY(map_2d(&L.a1, xq, 1, c.d, c.T, 128, 128));
+    MOE_TRY(map_3d(&L.b1, w->ws13, 1, c.d, 2 * (uint64_t)c.I, c.S, 128, 64));
+    L.p.rows1 = c.T;
+    L.p.n_tiles1 = c.S * c.I / 128;
+    L.p.k_blocks1 = c.d / 128;
+    L.p.a_scale1 = xq_scale;
+    L.p.b_scale1 = w->ws13_scale;
+    L.p.out1 = at<void>(ws, Lw.hs);
+    L.p.out_scale1 = at<float>(ws, Lw.hs_scale);
+    L.p.ldo1 = c.S * c.I;
+    tiles += (long long)((c.T + 127) / 128) * L.p.n_tiles1;
+  }
+  if (tiles == 0) return MOE_OK;
+  if (!routed) {
+    L.a0 = L.a1;
+    L.b0 = L.b1;
+  }
+  if (!(shared && c.S > 0)) {
+    L.a1 = L.a0;
+    L.b1 = L.b0;
+  }
+  L.p.I = c.I;
+  L.p.N = c.d;
+  L.p.err = at<int>(ws, 0);
+  L.grid = tc_grid(tiles);
+  L.stream = st;
+  MOE_CUDA(launch_fp8_gemm(L));
+  return MOE_OK;
+}
+
+moe_status fp8_gemm2(const moe_config& c, const int32_t* offsets, const moe_weights* w, void* yp, bool shared,
+                     const void* radd, void* out, void* ws, cudaStream_t st) {
+  const Layout Lw = layout(c);
+  const int TK = c.T * c.K;
+  Fp8GemmLaunch L{};
+  if (!shared) {
+    L.epi = Fp8Epi::kStore;
+    MOE_TRY(map_2d(&L.a0, at<void>(ws, Lw.h), 1, c.I, TK, 128, 128));
+    MOE_TRY(map_3d(&L.b0, w->w2, 1, c.I, c.d, c.E, 128, 256));
+    L.a1 = L.a0;
+    L.b1 = L.b0;
+    L.p.groups0 = c.E;
+    L.p.offsets0 = offsets;
+    L.p.rows_total0 = TK;
+    L.p.n_tiles0 = c.d / 256;
+    L.p.k_blocks0 = c.I / 128;
+    L.p.a_scale0 = at<float>(ws, Lw.h_scale);
+    L.p.b_scale0 = w->w2_scale;
+    L.p.out0 = yp;
+    L.p.ldo0 = c.d;
+    L.grid = tc_grid(((long long)TK / 128 + c.E) * L.p.n_tiles0);
+  } else {
+    L.epi = Fp8Epi::kCombine;
+    MOE_TRY(map_2d(&L.a1, at<void>(ws, Lw.hs), 1, (uint64_t)c.S * c.I, c.T, 128, 128));
+    MOE_TRY(map_3d(&L.b1, w->ws2, 1, c.I, c.d, c.S, 128, 256));
+    L.a0 = L.a1;
+    L.b0 = L.b1;
+    L.p.groups0 = 0;
+    L.p.rows1 = c.T;
+    L.p.n_tiles1 = c.d / 256;
+    L.p.k_blocks1 = c.S * c.I / 128;
+    L.p.a_scale1 = at<float>(ws, Lw.hs_scale);
+    L.p.b_scale1 = w->ws2_scale;
+    L.p.out1 = out;
+    L.p.ldo1 = c.d;
+    L.p.radd = static_cast<const __nv_bfloat16*>(radd);
+    L.grid = tc_grid((long long)((c.T + 127) / 128) * L.p.n_tiles1);
+  }
+  L.p.I = c.I;
+  L.p.N = c.d;
+  L.p.err = at<int>(ws, 0);
+  L.stream = st;
+  MOE_CUDA(launch_fp8_gemm(L));
+  return MOE_OK;
+}
+
 // GEMM1 (SwiGLU) of the routed experts over xp and/or the shared experts over x.
-moe_status gemm1_stage(const moe_config& c, const void* xp, const int32_t* offsets, const void* x,
-                       const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st) {
+moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
+                       const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st) {
   const Layout Lw = layout(c);
   const int TK = c.T * c.K;
   if (c.act == MOE_F32) {
@@ -272,7 +375,10 @@ moe_status gemm1_stage(const moe_config& c, const void* xp, const int32_t* offse
     }
     return MOE_OK;
   }
-  if (c.expert == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (c.expert == MOE_E4M3) {
+    return fp8_gemm1(c, xp, xp_scale, offsets, at<uint8_t>(ws, Lw.xq), at<float>(ws, Lw.xq_scale), w, routed,
+                     shared, ws, st);
+  }
   TcGemmLaunch L{};
   L.epi = Epi::kSwiGLU;
   L.bn = 256;
@@ -336,7 +442,7 @@ moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const
     MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(TK, c.E), st));
     return MOE_OK;
   }
-  if (c.expert == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (c.expert == MOE_E4M3) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kStore;
   L.bn = down_bn(c.d);
@@ -364,7 +470,11 @@ moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_
                                const moe_weights* w, void* out, void* ws, cudaStream_t st) {
   const Layout Lw = layout(c);
   if (c.S == 0) {
-    MOE_CUDA(launch_gather_combine(yp, slot_pos, gate, c.T, c.d, c.K, c.act == MOE_BF16, out, num_sms(), st));
+    if (c.act == MOE_BF16) {
+      MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, out, num_sms(), st));
+    } else {
+      MOE_CUDA(launch_gather_combine(yp, slot_pos, gate, c.T, c.d, c.K, false, out, num_sms(), st));
+    }
     return MOE_OK;
   }
   if (c.act == MOE_F32) {
@@ -387,7 +497,11 @@ moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_
     MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(c.T, 0), st));
     return MOE_OK;
   }
-  if (c.expert == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  // routed sum r[t] (in the xp region of the workspace: the permuted rows are
+  // dead once the routed GEMM1 has run), added by the down projection's epilogue
+  void* r = at<void>(ws, Lw.xp);
+  MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, r, num_sms(), st));
+  if (c.expert == MOE_E4M3) return fp8_gemm2(c, nullptr, w, nullptr, true, r, out, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kCombine;
   L.bn = down_bn(c.d);
@@ -402,10 +516,7 @@ moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_
   L.p.out1 = out;
   L.p.ldo1 = c.d;
   L.p.I = c.I;
-  L.p.slot_pos = slot_pos;
-  L.p.gate = gate;
-  L.p.yp = static_cast<const __nv_bfloat16*>(yp);
-  L.p.topk = c.K;
+  L.p.radd = static_cast<const __nv_bfloat16*>(r);
   L.p.err = at<int>(ws, 0);
   L.grid = tc_grid((long long)((c.T + 127) / 128) * L.p.n_tiles1);
   L.stream = st;
@@ -484,7 +595,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const float* x
   if (!ok_ptr(xp) || !ok_ptr(offsets) || !ok_ptr(yp)) return MOE_ERR_INVALID_ARG;
   if (c.expert == MOE_E4M3 && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  MOE_TRY(gemm1_stage(c, xp, offsets, nullptr, w, true, false, ws, st));
+  MOE_TRY(gemm1_stage(c, xp, xp_scale, offsets, nullptr, w, true, false, ws, st));
   MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
   return MOE_OK;
 }
@@ -499,7 +610,14 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
   if (!ok_ptr(yp) || !ok_ptr(slot_pos) || !ok_ptr(topk_gate) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
   if (c.S > 0 && !ok_ptr(x)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (c.S > 0) MOE_TRY(gemm1_stage(c, nullptr, nullptr, x, w, false, true, ws, st));
+  if (c.S > 0) {
+    if (c.expert == MOE_E4M3) {
+      const Layout Lw = layout(c);
+      MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
+                                    at<float>(ws, Lw.xq_scale), num_sms(), st));
+    }
+    MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, st));
+  }
   MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));
   return MOE_OK;
 }
@@ -545,7 +663,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
                           f8 ? at<float>(ws, Lw.xp_scale) : nullptr, f8 ? at<uint8_t>(ws, Lw.xq) : nullptr,
                           f8 ? at<float>(ws, Lw.xq_scale) : nullptr, ws, st));
     MOE_TRY(stage_mark(3, st));
-    MOE_TRY(gemm1_stage(c, xp, offsets, x, w, true, true, ws, st));
+    MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, true, ws, st));
     MOE_TRY(stage_mark(4, st));
     MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
     MOE_TRY(stage_mark(5, st));

@@ -1,0 +1,97 @@
+// Tile scheduler and epilogue helpers shared by the tcgen05 GEMM kernels.
+//
+// The tiles of a launch are numbered 0..total-1: first those of segment 0
+// (groups with device-side row offsets, group by group), then those of
+// segment 1 (one group of rows1 rows). Inside a group the m-tiles are taken
+// in super-rows of kSuperRow: for each n-tile the super-row's m-tiles come
+// one after the other, so that the CTAs running at the same time share the
+// B panel (weights) and reuse the super-row's A panels from L2.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;          // tile rows (one TMEM lane per row)
+constexpr int kSuperRow = 16;     // m-tiles walked together per n sweep
+constexpr int kMaxGroups = 512;
+
+struct Tile {
+  int seg, group, m, n, row0, row_end;
+};
+
+struct Sched {
+  const int* tp;    // [groups0 + 1] first tile of each group (shared memory)
+  const int* mt;    // [groups0] m-tiles of each group
+  const int* off;   // [groups0 + 1] row offsets
+  int groups0, tiles0, total;
+  int n_tiles0, n_tiles1, mt1, rows1;
+
+  __device__ __forceinline__ static void raster(int local, int mt, int nt, int& m, int& n) {
+    const int sr = local / (kSuperRow * nt);
+    const int base = sr * kSuperRow;
+    const int h = min(kSuperRow, mt - base);
+    const int rem = local - sr * kSuperRow * nt;
+    n = rem / h;
+    m = base + rem % h;
+  }
+
+  __device__ __forceinline__ Tile decode(int L) const {
+    Tile t;
+    if (L < tiles0) {
+      int lo = 0, hi = groups0;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tp[mid] <= L) lo = mid; else hi = mid;
+      }
+      t.seg = 0;
+      t.group = lo;
+      raster(L - tp[lo], mt[lo], n_tiles0, t.m, t.n);
+      t.row0 = off[lo] + t.m * kBM;
+      t.row_end = off[lo + 1];
+    } else {
+      t.seg = 1;
+      t.group = 0;
+      raster(L - tiles0, mt1, n_tiles1, t.m, t.n);
+      t.row0 = t.m * kBM;
+      t.row_end = rows1;
+    }
+    return t;
+  }
+};
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+    w.x = *reinterpret_cast<uint32_t*>(&h0);
+    w.y = *reinterpret_cast<uint32_t*>(&h1);
+    w.z = *reinterpret_cast<uint32_t*>(&h2);
+    w.w = *reinterpret_cast<uint32_t*>(&h3);
+    d4[q] = w;
+  }
+}
+
+__device__ __forceinline__ void add_bf16x32(float* acc, const __nv_bfloat16* src, float g) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = __ldg(s4 + q);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = __bfloat1622float2(h[j]);
+      acc[8 * q + 2 * j + 0] = fmaf(g, f.x, acc[8 * q + 2 * j + 0]);
+      acc[8 * q + 2 * j + 1] = fmaf(g, f.y, acc[8 * q + 2 * j + 1]);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe

@@ -132,7 +132,58 @@ __global__ void gather_combine_kernel(const Tv* __restrict__ yp, const int* __re
   }
 }
 
+// r[t] = sum_k gate[t,k] * yp[slot_pos[t,k]] for bf16 rows: one warp per
+// token, 16-byte loads of the K routed rows (each a contiguous row of yp),
+// fp32 sums, one 16-byte bf16 store per 8 columns.
+__global__ void __launch_bounds__(256) routed_sum_bf16_kernel(const uint4* __restrict__ yp,
+                                                              const int* __restrict__ slot_pos,
+                                                              const float* __restrict__ gate, int T, int row_vecs,
+                                                              int topk, uint4* __restrict__ r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8) {
+    int pos = 0;
+    float g = 0.0f;
+    if (lane < topk) {
+      pos = slot_pos[(size_t)t * topk + lane];
+      g = gate[(size_t)t * topk + lane];
+    }
+    for (int i = lane; i < row_vecs; i += 32) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int k = 0; k < topk; ++k) {
+        const int pk = __shfl_sync(0xffffffffu, pos, k);
+        const float gk = __shfl_sync(0xffffffffu, g, k);
+        const uint4 w = __ldg(yp + (size_t)pk * row_vecs + i);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(h[j]);
+          acc[2 * j] = fmaf(gk, f.x, acc[2 * j]);
+          acc[2 * j + 1] = fmaf(gk, f.y, acc[2 * j + 1]);
+        }
+      }
+      uint4 o;
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&b0);
+      o.y = *reinterpret_cast<uint32_t*>(&b1);
+      o.z = *reinterpret_cast<uint32_t*>(&b2);
+      o.w = *reinterpret_cast<uint32_t*>(&b3);
+      r[(size_t)t * row_vecs + i] = o;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_routed_sum_bf16(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
+                                   void* r, int num_sms, cudaStream_t st) {
+  const int blocks = std::max(1, std::min((T + 7) / 8, num_sms * 16));
+  routed_sum_bf16_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(yp), slot_pos, gate, T, d / 8, topk,
+                                                 static_cast<uint4*>(r));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_simt_gemm(const SimtParams& p, int max_mtiles, cudaStream_t st) {
   if (max_mtiles <= 0) return cudaSuccess;

@@ -1,17 +1,15 @@
 // tcgen05 persistent grouped GEMM (bf16 x bf16 -> fp32 TMEM) with the MoE
 // epilogues: router sigmoid, SwiGLU, plain store, and the fused combine.
+#include "gemm_sched.cuh"
 #include "gemm_tc.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;          // tile rows (one TMEM lane per row)
 constexpr int kBK = 64;           // bf16 elements per 128-byte swizzle row
 constexpr int kUK = 16;           // K per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;     // 6 warps
-constexpr int kSuperRow = 16;     // m-tiles walked together per n sweep
-constexpr int kMaxGroups = 512;
 constexpr int kAuxBytes = 8192;
 constexpr int kRingBytes = 196608;
 
@@ -26,82 +24,6 @@ struct Cfg {
                                    : (2 * BN <= 256) ? 256 : 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes;
 };
-
-struct Tile {
-  int seg, group, m, n, row0, row_end;
-};
-
-struct Sched {
-  const int* tp;    // [groups0 + 1] first tile of each group (shared memory)
-  const int* mt;    // [groups0] m-tiles of each group
-  const int* off;   // [groups0 + 1] row offsets
-  int groups0, tiles0, total;
-  int n_tiles0, n_tiles1, mt1, rows1;
-
-  __device__ __forceinline__ static void raster(int local, int mt, int nt, int& m, int& n) {
-    const int sr = local / (kSuperRow * nt);
-    const int base = sr * kSuperRow;
-    const int h = min(kSuperRow, mt - base);
-    const int rem = local - sr * kSuperRow * nt;
-    n = rem / h;
-    m = base + rem % h;
-  }
-
-  __device__ __forceinline__ Tile decode(int L) const {
-    Tile t;
-    if (L < tiles0) {
-      int lo = 0, hi = groups0;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tp[mid] <= L) lo = mid; else hi = mid;
-      }
-      t.seg = 0;
-      t.group = lo;
-      raster(L - tp[lo], mt[lo], n_tiles0, t.m, t.n);
-      t.row0 = off[lo] + t.m * kBM;
-      t.row_end = off[lo + 1];
-    } else {
-      t.seg = 1;
-      t.group = 0;
-      raster(L - tiles0, mt1, n_tiles1, t.m, t.n);
-      t.row0 = t.m * kBM;
-      t.row_end = rows1;
-    }
-    return t;
-  }
-};
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-    w.x = *reinterpret_cast<uint32_t*>(&h0);
-    w.y = *reinterpret_cast<uint32_t*>(&h1);
-    w.z = *reinterpret_cast<uint32_t*>(&h2);
-    w.w = *reinterpret_cast<uint32_t*>(&h3);
-    d4[q] = w;
-  }
-}
-
-__device__ __forceinline__ void add_bf16x32(float* acc, const __nv_bfloat16* src, float g) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w = __ldg(s4 + q);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float2 f = __bfloat1622float2(h[j]);
-      acc[8 * q + 2 * j + 0] = fmaf(g, f.x, acc[8 * q + 2 * j + 0]);
-      acc[8 * q + 2 * j + 1] = fmaf(g, f.y, acc[8 * q + 2 * j + 1]);
-    }
-  }
-}
 
 template <int BN, Epi EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -372,30 +294,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld32(tbase + c * 32, v);
           if (valid) store_bf16x32(out + (size_t)row * p.ldo0 + t.n * BN + c * 32, v);
         }
-      } else {  // kCombine: shared-expert down projection + gate-weighted routed rows
+      } else {  // kCombine: shared-expert down projection + the routed sum
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out1);
-        constexpr int kMaxK = 32;
-        int pos[kMaxK];
-        float gw[kMaxK];
-        if (valid) {
-#pragma unroll
-          for (int k = 0; k < kMaxK; ++k) {
-            if (k < p.topk) {
-              pos[k] = __ldg(p.slot_pos + (size_t)row * p.topk + k);
-              gw[k] = __ldg(p.gate + (size_t)row * p.topk + k);
-            }
-          }
-        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           ptx::tmem_ld32(tbase + c * 32, v);
           if (valid) {
-            const int col = t.n * BN + c * 32;
-#pragma unroll
-            for (int k = 0; k < kMaxK; ++k) {
-              if (k < p.topk) add_bf16x32(v, p.yp + (size_t)pos[k] * p.ldo1 + col, gw[k]);
-            }
-            store_bf16x32(out + (size_t)row * p.ldo1 + col, v);
+            const size_t o = (size_t)row * p.ldo1 + t.n * BN + c * 32;
+            add_bf16x32(v, p.radd + o, 1.0f);
+            store_bf16x32(out + o, v);
           }
         }
       }

@@ -30,7 +30,7 @@ enum class Epi : int {
   kRouterSigmoid = 0,  // out fp32 [rows, n_valid] = sigmoid(acc)
   kSwiGLU = 1,         // out bf16 [rows, ldo] = silu(gate) * up  (128 cols per tile)
   kStore = 2,          // out bf16 [rows, ldo] = acc
-  kCombine = 3,        // out bf16 [T, ldo] = acc + sum_k gate * yp[slot_pos]
+  kCombine = 3,        // out bf16 [T, ldo] = acc + radd (the gate-weighted routed sum)
 };
 
 struct TcGemmParams {
@@ -44,11 +44,9 @@ struct TcGemmParams {
   void* out1;
   int ldo0, ldo1;       // output row strides (elements)
   int n_valid;          // router: number of experts (output columns)
-  // kCombine
-  const int* slot_pos;  // [T, topk]
-  const float* gate;    // [T, topk]
-  const __nv_bfloat16* yp;  // [T*topk, ldo1]
-  int topk;
+  // kCombine: per-token routed sum r[t] = sum_k gate[t,k] * yp[slot_pos[t,k]],
+  // [T, ldo1] bf16, added to the shared experts' output in the epilogue
+  const __nv_bfloat16* radd;
   int* err;             // device error word
 };
 

@@ -61,6 +61,8 @@ struct SimtParams {
 
 cudaError_t launch_simt_gemm(const SimtParams& p, int max_mtiles, cudaStream_t st);
 int simt_max_mtiles(int rows_total, int groups);
+cudaError_t launch_routed_sum_bf16(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
+                                   void* r, int num_sms, cudaStream_t st);
 cudaError_t launch_gather_combine(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
                                   bool bf16, void* out, int num_sms, cudaStream_t st);
 

@@ -342,20 +342,19 @@ def quantize_blocks_128x128(w: np.ndarray):
     """128x128 blocks of a [n, k] weight matrix.
 
     Returns (q values float64 [n, k], scales fp32 [ceil(n/128), ceil(k/128)]).
+    The matrix is zero-padded to whole blocks (padding does not change a
+    block's amax) and viewed as [n/128, 128, k/128, 128]; each block gets
+    scale = amax / 448 and codes e4m3(w / scale).
     """
     w = np.asarray(w, F32)
     n, k = w.shape
     nbn, nbk = (n + 127) // 128, (k + 127) // 128
-    q = np.empty((n, k), dtype=F64)
-    scales = np.empty((nbn, nbk), dtype=F32)
-    for i in range(nbn):
-        for j in range(nbk):
-            blk = w[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
-            sc = tile_scale(np.abs(blk).max())
-            scales[i, j] = sc
-            q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128] = e4m3_value(
-                (blk / sc).astype(F32))
-    return q, scales
+    pad = np.zeros((nbn * 128, nbk * 128), F32)
+    pad[:n, :k] = w
+    blocks = pad.reshape(nbn, 128, nbk, 128)
+    scales = tile_scale(np.abs(blocks).max(axis=(1, 3)))
+    q = e4m3_value((blocks / scales[:, None, :, None]).astype(F32))
+    return q.reshape(nbn * 128, nbk * 128)[:n, :k], scales
 
 
 def fp8_gemm(qa, sa, qw, sw):
@@ -402,7 +401,7 @@ def layer_forward_fp8(x, topk_idx, topk_gate, wq, shared_wq):
     the same as the bf16 layer's (the router GEMM is not in FP8).
     """
     qx, sx = quantize_rows_1x128(np.asarray(x, F32))
-    out = np.zeros((x.shape[0], shared_wq[0][2].shape[0]), dtype=F64)
+    out = np.zeros(np.asarray(x).shape, dtype=F64)  # every expert maps width d back to d
     for (q13, s13, q2, s2) in shared_wq:
         out += swiglu_ffn_fp8(qx, sx, q13, s13, q2, s2)
     for e in np.unique(topk_idx):
@@ -410,3 +409,17 @@ def layer_forward_fp8(x, topk_idx, topk_gate, wq, shared_wq):
         y = swiglu_ffn_fp8(qx[rows], sx[rows], *wq[int(e)])
         out[rows] += np.asarray(topk_gate, F64)[rows, slots][:, None] * y
     return out
+
+
+def layer_forward_fp8_full(x, w_router, w13, w2, ws13, ws2, bias, G, K, M, group_topk=2):
+    """The FP8 layer on the rows of x: bf16-path routing (router_scores,
+    select_experts), then 128x128 block quantisation of the master weights of
+    every expert the rows use and of the shared experts, then the e4m3 expert
+    path of layer_forward_fp8. w13 / w2 / ws13 / ws2 are indexable stacks of
+    per-expert master weights."""
+    s = router_scores(x, w_router)
+    idx, gate = select_experts(s, bias, G, K, M, group_topk)
+    wq = {int(e): quantize_expert_weights(w13[int(e)], w2[int(e)]) for e in np.unique(idx)}
+    shared = [quantize_expert_weights(ws13[i], ws2[i]) for i in range(ws13.shape[0])]
+    out = layer_forward_fp8(np.asarray(x, F32), idx, gate, wq, shared)
+    return {"scores": s, "topk_idx": idx, "topk_gate": gate, "out": out}

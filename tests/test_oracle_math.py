@@ -241,3 +241,19 @@ def test_quantize_blocks_layout(shape):
             np.testing.assert_array_equal(
                 q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128],
                 om.e4m3_value((blk / sc[i, j]).astype(F32)))
+
+
+def test_fp8_layer_without_shared_experts():
+    """S = 0: the FP8 layer is the gate-weighted routed sum alone."""
+    rng = np.random.default_rng(14)
+    T, d, I = 4, 128, 128
+    x = rng.standard_normal((T, d)).astype(F32)
+    w13 = (rng.standard_normal((2, 2 * I, d)) * 0.05).astype(F32)
+    w2 = (rng.standard_normal((2, d, I)) * 0.05).astype(F32)
+    idx = np.array([[0, 1]] * T, np.int32)
+    gate = np.full((T, 2), 0.5, F32)
+    wq = {e: om.quantize_expert_weights(w13[e], w2[e]) for e in range(2)}
+    out = om.layer_forward_fp8(x, idx, gate, wq, [])
+    qx, sx = om.quantize_rows_1x128(x)
+    want = sum(0.5 * om.swiglu_ffn_fp8(qx, sx, *wq[e]) for e in range(2))
+    np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-13)
