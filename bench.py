@@ -261,6 +261,7 @@ def run_reference(a, p):
 # ---------------------------------------------------------------- our arm
 def run_ours(a, p):
     from mixture_experts_layer_100_b300 import binding as B
+    from mixture_experts_layer_100_b300 import dp
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -275,7 +276,6 @@ def run_ours(a, p):
     x = synth.make_x(p.replace(seed=p.seed + rank) if rank else p, w.w_router, device=dev)
     bias = synth.make_bias(p, device=dev)
     cfg = B.config_from_preset(p)
-    cfg_global = B.config_from_preset(p, T=p.T * world)
     ws = B.alloc_workspace(cfg, dev)
     wd = {k: getattr(w, k).contiguous() for k in ("w_router", "w13", "w2", "ws13", "ws2")}
     weights = B.make_weights(**wd)
@@ -286,15 +286,17 @@ def run_ours(a, p):
     mom = torch.empty(1, dtype=torch.float32, device=dev)
     gamma = p.gamma
 
-    def step():
+    update = dp.device_bias_update(cfg, gamma, bias, mom)
+
+    def step(xin=None):
+        xin = x if xin is None else xin
         if world == 1:
-            B.moe_layer_forward(cfg, x, weights, bias, gamma, out, idx, gate, counts, mom, ws)
+            B.moe_layer_forward(cfg, xin, weights, bias, gamma, out, idx, gate, counts, mom, ws)
         else:
             # the bias sees the load of the whole data-parallel batch: counts
             # are summed over ranks (1 KB all-reduce) before the update
-            B.moe_layer_forward(cfg, x, weights, bias, 0.0, out, idx, gate, counts, mom, ws)
-            pg.all_reduce(counts)
-            B.moe_bias_update(cfg_global, counts, gamma, bias, mom)
+            B.moe_layer_forward(cfg, xin, weights, bias, 0.0, out, idx, gate, counts, mom, ws)
+            dp.global_bias_update(counts, p.T, update)
 
     for _ in range(a.warmup):
         step()
@@ -373,12 +375,7 @@ def run_ours(a, p):
         e0.record()
         for _ in range(n):
             xd.copy_(xh, non_blocking=True)
-            if world == 1:
-                B.moe_layer_forward(cfg, xd, weights, bias, gamma, out, idx, gate, counts, mom, ws)
-            else:
-                B.moe_layer_forward(cfg, xd, weights, bias, 0.0, out, idx, gate, counts, mom, ws)
-                pg.all_reduce(counts)
-                B.moe_bias_update(cfg_global, counts, gamma, bias, mom)
+            step(xd)
             oh.copy_(out, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()

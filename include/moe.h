@@ -212,6 +212,12 @@ moe_status moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, co
  * combine, 7 after the bias update. count must be 0 (hook off) or >= 8. */
 moe_status moe_set_stage_events(void* const* events, int count);
 
+/* Self-test of the device-side wait bound: queues one small kernel that waits
+ * on an on-chip barrier nothing will release. The wait gives up after about a
+ * second, records MOE_ERR_TIMEOUT's device code (0x105) in the error word of
+ * `ws` and the kernel exits; read it with moe_device_error. */
+moe_status moe_selftest_timeout(void* ws, moe_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word in `ws`.
  * *code receives 0 when no device-side check has fired since the last call;
  * the return value is MOE_ERR_TIMEOUT / MOE_ERR_DEVICE when one has. */

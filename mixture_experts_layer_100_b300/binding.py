@@ -59,6 +59,7 @@ _SIGS = {
     "moe_quantize_weights_e4m3": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
     "moe_permute_static": [ctypes.POINTER(moe_config)] + [_P] * 7 + [_P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
+    "moe_selftest_timeout": [_P, _P],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
     "moe_status_string": [ctypes.c_int],
 }
@@ -170,6 +171,10 @@ def moe_set_stage_events(events) -> None:
         return
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("moe_set_stage_events", lib.moe_set_stage_events(arr, len(events)))
+
+
+def moe_selftest_timeout(ws, stream=None) -> None:
+    _check("moe_selftest_timeout", lib.moe_selftest_timeout(_ptr(ws), _stream(stream)))
 
 
 def moe_device_error(ws, stream=None) -> int:

@@ -15,12 +15,14 @@ enum DevErr : int {
   kDevTimeoutMma = 0x102,        // MMA issuer gave up waiting for data / TMEM
   kDevTimeoutEpilogue = 0x103,   // epilogue gave up waiting for an accumulator
   kDevTimeoutDrain = 0x104,      // exit-time wait for in-flight copies ran out
+  kDevTimeoutSelfTest = 0x105,   // moe_selftest_timeout: the wait ran out as intended
   kDevBadExpertIndex = 0x201,    // topk_idx entry outside [0, E)
   kDevCountMismatch = 0x202,     // counts[] is not the histogram of topk_idx
 };
 
 // A device-side wait that sees no progress for this long gives up.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;  // 1 s
+constexpr long long kWaitTimeoutCycles = 8000000000ll;          // 4 s at 2 GHz: backstop only
 
 struct __align__(16) bf16x8 {
   __nv_bfloat162 v[4];

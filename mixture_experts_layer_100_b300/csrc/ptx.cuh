@@ -60,17 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up
-// (returns false) after kWaitTimeoutNs without completion, or as soon as the
-// kernel's error word is set by another thread.
+// (returns false) after kWaitTimeoutNs without completion (with an SM-cycle
+// count as a second bound in case the global timer does not advance), or as
+// soon as the kernel's error word is set by another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const long long c0 = clock64();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (read_error(err) != 0) return false;
     if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if (clock64() - c0 > kWaitTimeoutCycles) return false;
   }
 }
 

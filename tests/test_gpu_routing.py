@@ -185,3 +185,21 @@ def test_bias_trajectory_bit_exact(name, steps, T):
         np.testing.assert_array_equal(bd.cpu().numpy(), biases[i])
         assert mom.item() == loads[i]
     assert loads[-1] < loads[0]
+
+
+def test_device_wait_gives_up_and_reports_timeout():
+    """A wait on a barrier that nothing releases returns after about a second
+    with a timeout code; the context stays usable afterwards."""
+    import time
+    Bn = B()
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    t0 = time.time()
+    Bn.moe_selftest_timeout(ws)
+    code = Bn.moe_device_error(ws)
+    assert code == 0x105 and time.time() - t0 < 30
+    assert Bn.moe_device_error(ws) == 0
+    # the GPU still runs work
+    s = synth.make_scores(64, 16, seed=9)
+    cfg = Bn.make_config(64, 128, 16, 4, 4, 2, 128, 1, 2, act="f32")
+    idx, _, _ = _route_gpu(cfg, s, torch.zeros(16))
+    np.testing.assert_array_equal(idx, om.select_experts(s.numpy(), np.zeros(16, np.float32), 4, 4, 2)[0])
