@@ -391,7 +391,7 @@ def run_ours(a, p):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        unit = CpuOracleUnit(p, w, x.cpu(), nt=p.T, rows=2048, n_experts=4)
+        unit = CpuOracleUnit(p, w, x.cpu(), nt=p.T, rows=2048, n_experts=min(32, p.E))
         v, secs = unit.run()
         cpu = {"value": v, "unit": "tokens/s", "cores": CpuOracleUnit.cores(), "kind": "oracle",
                "sample": unit.desc, "seconds": secs}

@@ -134,7 +134,10 @@ __global__ void gather_combine_kernel(const Tv* __restrict__ yp, const int* __re
 
 // r[t] = sum_k gate[t,k] * yp[slot_pos[t,k]] for bf16 rows: one warp per
 // token, 16-byte loads of the K routed rows (each a contiguous row of yp),
-// fp32 sums, one 16-byte bf16 store per 8 columns.
+// fp32 sums, one 16-byte bf16 store per 8 columns. All K loads of a column
+// chunk are issued before the first is used (KMAX >= topk, unrolled), so a
+// lane keeps K requests in flight.
+template <int KMAX>
 __global__ void __launch_bounds__(256) routed_sum_bf16_kernel(const uint4* __restrict__ yp,
                                                               const int* __restrict__ slot_pos,
                                                               const float* __restrict__ gate, int T, int row_vecs,
@@ -147,18 +150,29 @@ __global__ void __launch_bounds__(256) routed_sum_bf16_kernel(const uint4* __res
       pos = slot_pos[(size_t)t * topk + lane];
       g = gate[(size_t)t * topk + lane];
     }
-    for (int i = lane; i < row_vecs; i += 32) {
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int k = 0; k < topk; ++k) {
-        const int pk = __shfl_sync(0xffffffffu, pos, k);
-        const float gk = __shfl_sync(0xffffffffu, g, k);
-        const uint4 w = __ldg(yp + (size_t)pk * row_vecs + i);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+    int pk[KMAX];
+    float gk[KMAX];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(h[j]);
-          acc[2 * j] = fmaf(gk, f.x, acc[2 * j]);
-          acc[2 * j + 1] = fmaf(gk, f.y, acc[2 * j + 1]);
+    for (int k = 0; k < KMAX; ++k) {
+      pk[k] = __shfl_sync(0xffffffffu, pos, k);
+      gk[k] = __shfl_sync(0xffffffffu, g, k);
+    }
+    for (int i = lane; i < row_vecs; i += 32) {
+      uint4 w[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (k < topk) w[k] = __ldg(yp + (size_t)pk[k] * row_vecs + i);
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (k < topk) {
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            acc[2 * j] = fmaf(gk[k], f.x, acc[2 * j]);
+            acc[2 * j + 1] = fmaf(gk[k], f.y, acc[2 * j + 1]);
+          }
         }
       }
       uint4 o;
@@ -180,8 +194,15 @@ __global__ void __launch_bounds__(256) routed_sum_bf16_kernel(const uint4* __res
 cudaError_t launch_routed_sum_bf16(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
                                    void* r, int num_sms, cudaStream_t st) {
   const int blocks = std::max(1, std::min((T + 7) / 8, num_sms * 16));
-  routed_sum_bf16_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(yp), slot_pos, gate, T, d / 8, topk,
-                                                 static_cast<uint4*>(r));
+  const uint4* y = static_cast<const uint4*>(yp);
+  uint4* o = static_cast<uint4*>(r);
+  if (topk <= 8) {
+    routed_sum_bf16_kernel<8><<<blocks, 256, 0, st>>>(y, slot_pos, gate, T, d / 8, topk, o);
+  } else if (topk <= 16) {
+    routed_sum_bf16_kernel<16><<<blocks, 256, 0, st>>>(y, slot_pos, gate, T, d / 8, topk, o);
+  } else {
+    routed_sum_bf16_kernel<32><<<blocks, 256, 0, st>>>(y, slot_pos, gate, T, d / 8, topk, o);
+  }
   return cudaGetLastError();
 }
 
