@@ -68,7 +68,9 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
 typedef struct {
   int T, d, E, G, K, M, I, S;
   int group_topk;     /* group score = sum of this many largest biased
-                         affinities in the group (2 in DeepSeek-V3 shapes) */
+                         affinities in the group, added largest first
+                         (2 in DeepSeek-V3 shapes; E/G gives the plain sum
+                         over the group's experts, the pages' node score) */
   moe_dtype act;      /* x, out, router weights, yp: MOE_F32 or MOE_BF16 */
   moe_dtype expert;   /* expert GEMM operands: == act, or MOE_E4M3 with act
                          MOE_BF16 (1x128 activation tiles, 128x128 weight

@@ -84,7 +84,7 @@ moe_status check_config(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->E % c->G != 0 || c->G > 32 || c->M > c->G) return MOE_ERR_INVALID_ARG;
   const int gsz = c->E / c->G;
-  if (c->group_topk < 1 || c->group_topk > 4 || c->group_topk > gsz) return MOE_ERR_INVALID_ARG;
+  if (c->group_topk < 1 || c->group_topk > gsz) return MOE_ERR_INVALID_ARG;
   if (c->K > 32 || c->K > c->M * gsz) return MOE_ERR_INVALID_ARG;
   if (c->E > 512) return MOE_ERR_UNSUPPORTED;
   if (c->act != MOE_F32 && c->act != MOE_BF16) return MOE_ERR_INVALID_ARG;

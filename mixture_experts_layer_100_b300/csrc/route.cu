@@ -65,20 +65,43 @@ __global__ void __launch_bounds__(kWarps * 32)
     // group score: sum of the gk largest s' of the group, largest first
     float gs = -INFINITY;
     if (lane < G) {
-      float top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      for (int j = 0; j < gsz; ++j) {
-        float x = sp[lane * gsz + j];
+      const float* grp = sp + lane * gsz;
+      if (gk <= 4) {
+        float top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int j = 0; j < gsz; ++j) {
+          float x = grp[j];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          if (r < gk && x > top[r]) {
-            const float tmp = top[r];
-            top[r] = x;
-            x = tmp;
+          for (int r = 0; r < 4; ++r) {
+            if (r < gk && x > top[r]) {
+              const float tmp = top[r];
+              top[r] = x;
+              x = tmp;
+            }
           }
         }
+        gs = top[0];
+        for (int r = 1; r < gk; ++r) gs = __fadd_rn(gs, top[r]);
+      } else {
+        // larger gk (up to the whole group, the plain node sum): take the
+        // members in (value desc, index asc) order one at a time
+        float last_v = INFINITY;
+        int last_j = -1;
+        for (int r = 0; r < gk; ++r) {
+          float bv = -INFINITY;
+          int bj = gsz;
+          for (int j = 0; j < gsz; ++j) {
+            const float x = grp[j];
+            const bool after_last = x < last_v || (x == last_v && j > last_j);
+            if (after_last && (x > bv || (x == bv && j < bj))) {
+              bv = x;
+              bj = j;
+            }
+          }
+          gs = r == 0 ? bv : __fadd_rn(gs, bv);
+          last_v = bv;
+          last_j = bj;
+        }
       }
-      gs = top[0];
-      for (int r = 1; r < gk; ++r) gs = __fadd_rn(gs, top[r]);
     }
     // the M best groups (ties: lower group index)
     int rank = 0;

@@ -25,6 +25,8 @@ SMALL = {
     "t1_d256_e16": dict(T=1, d=256, E=16, G=4, K=4, M=2, I=128, S=1),
     "t700_d128_e256_k8": dict(T=700, d=128, E=256, G=8, K=8, M=4, I=128, S=1),
     "t129_d512_e64_s0": dict(T=129, d=512, E=64, G=8, K=6, M=3, I=256, S=0),
+    "t200_d256_e128_k6": dict(T=200, d=256, E=128, G=8, K=6, M=3, I=128, S=1),
+    "t333_d256_e32_nodesum": dict(T=333, d=256, E=32, G=4, K=4, M=2, I=128, S=1, group_topk=8),
 }
 
 
@@ -228,3 +230,53 @@ def test_v3_decode_presets(v3_weights, name, sample):
     res = run_layer(p, device_weights(w), x, b.to(DEV))
     toks = None if sample is None else np.sort(np.random.default_rng(2).choice(p.T, sample, replace=False))
     compare(p, res, oracle_rows(p, w, x.cpu(), b, toks), b, tokens=toks, max_flip=0.05)
+
+
+def test_bias_checkpoint_resumes_bit_exactly():
+    """The layer's only state is the routing bias: saving it after 3 steps and
+    resuming from the saved copy gives the same trajectory as 6 straight steps."""
+    from mixture_experts_layer_100_b300 import state
+    p = small_preset("t300_d256_e16_i256")
+    w = synth.make_weights(p)
+    wd = device_weights(w)
+    x = synth.make_x(p, w.w_router).to(DEV)
+    b_run = synth.make_bias(p).to(DEV)
+    for _ in range(6):
+        run_layer(p, wd, x, b_run, gamma=p.gamma)
+    b_a = synth.make_bias(p).to(DEV)
+    for _ in range(3):
+        run_layer(p, wd, x, b_a, gamma=p.gamma)
+    blob = state.save_bias(b_a, step=3)
+    b_b, step = state.load_bias(blob, device=DEV)
+    assert step == 3
+    for _ in range(3):
+        run_layer(p, wd, x, b_b, gamma=p.gamma)
+    assert torch.equal(b_b, b_run)
+
+
+def test_fp8_preset_balancing_loop_on_the_layer():
+    """The FP8 preset's loop on the full layer: 50 forward + bias-update steps
+    on fixed inputs; every step each bias moves by exactly -gamma, +gamma or
+    0 against its expert's load, and the peak load comes down."""
+    from tests.layer_helpers import quantize_device_weights
+    p = synth.PRESETS["v3_t32768_d7168_e256_fp8"]
+    w = synth.make_weights(p, device=DEV)
+    wq = quantize_device_weights(device_weights(w))
+    del w
+    x = synth.make_x(p, wq["w_router"], device=DEV)
+    b = synth.make_bias(p).to(DEV)
+    g = np.float32(p.gamma)
+    loads = []
+    from mixture_experts_layer_100_b300 import binding as B
+    ws = B.alloc_workspace(B.config_from_preset(p))
+    for _ in range(p.steps):
+        prev = b.cpu().numpy().copy()
+        res = run_layer(p, wq, x, b, gamma=p.gamma, ws=ws)
+        c = res["counts"].cpu().numpy().astype(np.int64)
+        assert c.sum() == p.T * p.K
+        want = np.where(c * p.E > p.T * p.K, prev - g, np.where(c * p.E < p.T * p.K, prev + g, prev))
+        np.testing.assert_array_equal(b.cpu().numpy(), want.astype(np.float32))
+        loads.append(res["max_over_mean"].item())
+        assert loads[-1] == np.float32(c.max() * p.E / (p.T * p.K))
+    assert loads[-1] < loads[0], (loads[0], loads[-1])
+

@@ -42,6 +42,8 @@ ROUTE_SHAPES = [
     (8, 4, 2, 2, 2),
     (96, 6, 5, 2, 3),     # E not a multiple of 32, three-term group score
     (512, 32, 8, 4, 1),   # the largest supported expert count
+    (64, 4, 6, 2, 16),    # group score = plain sum over the group (the pages' node score)
+    (256, 8, 8, 4, 32),   # V3 shape with the plain node sum
 ]
 
 

@@ -82,7 +82,8 @@ def _brute_route_token(sp, G, K, M, gk):
 
 @pytest.mark.parametrize("E,G,K,M,gk", [(8, 4, 2, 2, 2), (12, 3, 3, 2, 2),
                                         (16, 4, 4, 2, 2), (16, 8, 3, 3, 2),
-                                        (12, 4, 2, 1, 1), (16, 4, 5, 3, 3)])
+                                        (12, 4, 2, 1, 1), (16, 4, 5, 3, 3),
+                                        (16, 4, 4, 2, 4), (12, 2, 3, 1, 6)])  # full group sums
 @pytest.mark.parametrize("kind", ["uniform", "dyadic"])
 def test_brute_force_selection(E, G, K, M, gk, kind):
     rng = np.random.default_rng(E * 100 + K * 10 + M)
@@ -227,3 +228,16 @@ def test_bias_update_moves_toward_balance():
 def test_load_max_over_mean():
     counts = np.array([4, 0, 2, 2], np.int32)  # T*K = 8, E = 4, mean 2
     assert om.load_max_over_mean(counts, 4, 2) == 2.0
+
+
+def test_bias_checkpoint_round_trip():
+    import torch
+    from mixture_experts_layer_100_b300 import state
+    b = torch.tensor([1e-3, -2e-3, 0.0, -0.0, 3.4e38, 1.17549435e-38], dtype=torch.float32)
+    blob = state.save_bias(b, step=42)
+    b2, step = state.load_bias(blob)
+    assert step == 42 and torch.equal(b2.view(torch.int32), b.view(torch.int32))
+    with pytest.raises(ValueError):
+        state.load_bias(b"XXXX" + blob[4:])
+    with pytest.raises(ValueError):
+        state.load_bias(blob[:-4])
