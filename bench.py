@@ -37,7 +37,8 @@ METRIC = "MoE-layer tokens/sec (1×B300, V3 shape T=16K bf16); % tensor/HBM roof
 DEFAULT_PRESET = "v3_t16384_d7168_e256_bf16"
 STAGES = ["router_gemm", "route_select", "permute", "gemm1_swiglu", "gemm2_routed", "gemm2_shared_combine",
           "bias_update"]
-KERNELS_PER_STEP = 10  # router, select, rank, scan, scatter, gemm1, gemm2, routed sum, gemm2+combine, bias
+KERNELS_PER_STEP = 11  # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, routed sum,
+#                        gemm2+combine, bias
 
 
 def parse():
@@ -139,23 +140,33 @@ def dist_env():
     return world, rank, local
 
 
-def traffic_from_profiles(kernel_file: str, key: str):
-    """DRAM bytes per launch recorded in profiles/ for the current source of
-    the kernel (None when the kernel source changed since the capture)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "mixture_experts_layer_100_b300", "csrc", kernel_file)
+TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_epi.cuh", "gemm_sched.cuh", "api.cu")
+
+
+def source_sha(files=TRAFFIC_SOURCES) -> str:
+    """Hash of the kernel and launch sources a traffic measurement depends on."""
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mixture_experts_layer_100_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(key: str):
+    """DRAM bytes per launch recorded in profiles/ for the current kernel and
+    launch sources (None when either changed since the capture)."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[key]
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        return rec["bytes_per_launch"] if rec.get("source_sha") == sha else None
+        return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha() else None
     except Exception:
         return None
 
 
 def flops_gemm1(p):
-    return 2.0 * (p.T * p.K + p.T * p.S) * p.d * 2 * p.I
+    """Routed experts' GEMM1 (the shared experts' GEMM1 runs on a side stream,
+    overlapped with routing and permutation, and is not in this stage)."""
+    return 2.0 * p.T * p.K * p.d * 2 * p.I
 
 
 def flops_gemm2_routed(p):
@@ -409,11 +420,11 @@ def run_ours(a, p):
         # FP8 dense peak: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
         tf_burst, tf_sust, src = 2 * tf_burst, 2 * tf_sust, src + " bf16 x 2 (nominal fp8 ratio)"
     g1 = flops_gemm1(p) / (stage_ms["gemm1_swiglu"] * 1e-3) / 1e12
-    roofline = {"kernel": "gemm1_swiglu (routed + shared experts, tcgen05)", "bound": "tensor",
+    roofline = {"kernel": "gemm1_swiglu (routed experts, tcgen05)", "bound": "tensor",
                 "achieved": g1, "peak": tf_sust, "unit": "TFLOP/s", "frac": g1 / tf_sust,
                 "peak_kind": f"{'fp8' if p.expert_dtype == 'e4m3' else 'bf16'} dense, sustained ({src})",
                 "frac_of_burst_peak": g1 / tf_burst,
-                "traffic": traffic_from_profiles("gemm_tc.cu", "gemm1_swiglu")}
+                "traffic": traffic_from_profiles("gemm1_swiglu")}
     stages = {}
     hb = hbm_bytes(p)
     for name in STAGES:

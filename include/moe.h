@@ -159,6 +159,11 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float g
 
 /* The whole layer: route, permute, routed experts, shared experts with the
  * fused combine, and (when gamma != 0) the bias update, queued on `stream`.
+ * The shared experts' first GEMM runs on an internal side stream (one per
+ * host thread and device, created by the first call and kept until the
+ * process exits) while `stream` routes and permutes; `stream` waits for it
+ * before the combine, so the layer is complete when `stream` is. Make the
+ * first call on a device outside stream capture.
  * out [T, d] in cfg->act; topk_idx, topk_gate, counts as in moe_route;
  * bias [E] fp32 is updated in place after routing when gamma != 0;
  * max_over_mean as in moe_bias_update (nullable). */

@@ -538,6 +538,29 @@ moe_status check_weights(const moe_config& c, const moe_weights* w, bool routed,
 
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
+// Side stream of moe_layer_forward (one per host thread and device, created
+// on first use and kept for the life of the process): the shared experts'
+// GEMM1 runs there while the main stream routes and permutes.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+moe_status side_stream(SideStream** out) {
+  thread_local SideStream cache[64];
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  SideStream& ss = cache[dev];
+  if (ss.s == nullptr) {
+    MOE_CUDA(cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking));
+    MOE_CUDA(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
+    MOE_CUDA(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+  }
+  *out = &ss;
+  return MOE_OK;
+}
+
 thread_local cudaEvent_t g_stage_events[8];
 thread_local bool g_stage_on = false;
 
@@ -649,8 +672,24 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
   MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
   if (c.T > 0) {
     float* scores = at<float>(ws, Lw.scores);
+    const bool f8 = c.expert == MOE_E4M3;
     MOE_TRY(router_scores(c, x, w->w_router, scores, ws, st));
     MOE_TRY(stage_mark(1, st));
+    // The shared experts' GEMM1 depends on x only: it runs on a side stream,
+    // overlapping the memory-bound selection and permutation below; the main
+    // stream waits for it before the shared down projection.
+    SideStream* side = nullptr;
+    if (c.S > 0) {
+      MOE_TRY(side_stream(&side));
+      MOE_CUDA(cudaEventRecord(side->fork, st));
+      MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+      if (f8) {
+        MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
+                                      at<float>(ws, Lw.xq_scale), num_sms(), side->s));
+      }
+      MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, side->s));
+      MOE_CUDA(cudaEventRecord(side->join, side->s));
+    }
     MOE_CUDA(launch_route_select(scores, bias, c.T, c.E, c.G, c.K, c.M, c.group_topk, topk_idx, topk_gate, counts,
                                  num_sms(), st));
     MOE_TRY(stage_mark(2, st));
@@ -658,15 +697,14 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
     int32_t* slot_pos = at<int32_t>(ws, Lw.slot_pos);
     void* xp = at<void>(ws, Lw.xp);
     void* yp = at<void>(ws, Lw.yp);
-    const bool f8 = c.expert == MOE_E4M3;
     MOE_TRY(permute_stage(c, topk_idx, counts, offsets, at<int32_t>(ws, Lw.sorted_tok), slot_pos, x, xp,
-                          f8 ? at<float>(ws, Lw.xp_scale) : nullptr, f8 ? at<uint8_t>(ws, Lw.xq) : nullptr,
-                          f8 ? at<float>(ws, Lw.xq_scale) : nullptr, ws, st));
+                          f8 ? at<float>(ws, Lw.xp_scale) : nullptr, nullptr, nullptr, ws, st));
     MOE_TRY(stage_mark(3, st));
-    MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, true, ws, st));
+    MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, false, ws, st));
     MOE_TRY(stage_mark(4, st));
     MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
     MOE_TRY(stage_mark(5, st));
+    if (side != nullptr) MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
     MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));
     MOE_TRY(stage_mark(6, st));
     if (gamma != 0.0f)
