@@ -38,7 +38,11 @@ Readings where the pages are silent (each is listed in the design notes):
     e4m3(v / scale) with round-to-nearest-even and saturation to +/-448;
     activations in 1x128 tiles along the contraction axis, weights in
     128x128 blocks; each 128-wide block partial product is scaled and summed
-    in float64.
+    in float64;
+  * FP8 with power-of-two scales (the UE8M0 mode, an option beside the
+    pages' fp32 scales): scale = the smallest power of two not below
+    amax / 448, kept inside UE8M0's range [2^-127, 2^127] (1 when amax == 0);
+    codes and GEMMs as above, so only the scale rule differs.
 """
 from __future__ import annotations
 
@@ -319,32 +323,59 @@ def tile_scale(amax):
     return np.where(amax > 0, sc, F32(1.0)).astype(F32)
 
 
-def quantize_rows_1x128(v: np.ndarray):
+def tile_scale_ue8m0(amax):
+    """Power-of-two scale of one tile: the smallest 2^e with 2^e >= amax / 448,
+    e clamped to [-127, 127] (the exponents a UE8M0 byte can hold), or 1 when
+    the tile is all zero. Returned as fp32 values (2^-127 is an fp32
+    subnormal, still exact).
+
+    amax / 448 is formed in float64; it is a power of two exactly when amax is
+    448 * 2^k (then the float64 quotient is exact), and otherwise lies at
+    least one fp32 ulp away from every power of two, far beyond the float64
+    rounding of the quotient, so frexp of the quotient decides e correctly.
+    """
+    amax = np.asarray(amax, F32).astype(F64)
+    r = amax / E4M3_MAX
+    m, ex = np.frexp(r)                      # r = m * 2^ex, m in [0.5, 1)
+    e = np.where(m == 0.5, ex - 1, ex)       # ceil(log2 r)
+    e = np.clip(e, -127, 127)
+    sc = np.ldexp(1.0, e).astype(F32)
+    return np.where(amax > 0, sc, F32(1.0)).astype(F32)
+
+
+def _scale_rule(ue8m0: bool):
+    return tile_scale_ue8m0 if ue8m0 else tile_scale
+
+
+def quantize_rows_1x128(v: np.ndarray, ue8m0: bool = False):
     """Per-row 1x128 tiles along the last axis.
 
     Returns (q values float64 [n, k] (e4m3 grid), scales fp32 [n, ceil(k/128)]).
-    q = e4m3(v / scale) with the division done in fp32.
+    q = e4m3(v / scale) with the division done in fp32; the scale follows
+    tile_scale, or tile_scale_ue8m0 when ue8m0 is set.
     """
     v = np.asarray(v, F32)
     n, k = v.shape
     nb = (k + 127) // 128
     q = np.empty((n, k), dtype=F64)
     scales = np.empty((n, nb), dtype=F32)
+    rule = _scale_rule(ue8m0)
     for b in range(nb):
         blk = v[:, b * 128:(b + 1) * 128]
-        sc = tile_scale(np.abs(blk).max(axis=1))
+        sc = rule(np.abs(blk).max(axis=1))
         scales[:, b] = sc
         q[:, b * 128:(b + 1) * 128] = e4m3_value((blk / sc[:, None]).astype(F32))
     return q, scales
 
 
-def quantize_blocks_128x128(w: np.ndarray):
+def quantize_blocks_128x128(w: np.ndarray, ue8m0: bool = False):
     """128x128 blocks of a [n, k] weight matrix.
 
     Returns (q values float64 [n, k], scales fp32 [ceil(n/128), ceil(k/128)]).
     The matrix is zero-padded to whole blocks (padding does not change a
     block's amax) and viewed as [n/128, 128, k/128, 128]; each block gets
-    scale = amax / 448 and codes e4m3(w / scale).
+    scale = amax / 448 (or tile_scale_ue8m0 when ue8m0 is set) and codes
+    e4m3(w / scale).
     """
     w = np.asarray(w, F32)
     n, k = w.shape
@@ -352,7 +383,7 @@ def quantize_blocks_128x128(w: np.ndarray):
     pad = np.zeros((nbn * 128, nbk * 128), F32)
     pad[:n, :k] = w
     blocks = pad.reshape(nbn, 128, nbk, 128)
-    scales = tile_scale(np.abs(blocks).max(axis=(1, 3)))
+    scales = _scale_rule(ue8m0)(np.abs(blocks).max(axis=(1, 3)))
     q = e4m3_value((blocks / scales[:, None, :, None]).astype(F32))
     return q.reshape(nbn * 128, nbk * 128)[:n, :k], scales
 
@@ -375,51 +406,55 @@ def fp8_gemm(qa, sa, qw, sw):
     return out
 
 
-def quantize_expert_weights(w13: np.ndarray, w2: np.ndarray):
+def quantize_expert_weights(w13: np.ndarray, w2: np.ndarray, ue8m0: bool = False):
     """128x128 block quantisation of one expert's W13 [2I, d] and W2 [d, I]."""
-    q13, s13 = quantize_blocks_128x128(w13)
-    q2, s2 = quantize_blocks_128x128(w2)
+    q13, s13 = quantize_blocks_128x128(w13, ue8m0)
+    q2, s2 = quantize_blocks_128x128(w2, ue8m0)
     return q13, s13, q2, s2
 
 
-def swiglu_ffn_fp8(qx, sx, q13, s13, q2, s2):
+def swiglu_ffn_fp8(qx, sx, q13, s13, q2, s2, ue8m0: bool = False):
     """One expert with e4m3 operands: GEMM1 on (qx, sx) x (q13, s13), SwiGLU in
-    float64, h rounded to fp32 and re-quantised in 1x128 tiles along I, then
-    GEMM2 on (qh, sh) x (q2, s2)."""
+    float64, h rounded to fp32 and re-quantised in 1x128 tiles along I (with
+    the same scale rule as the operands), then GEMM2 on (qh, sh) x (q2, s2)."""
     I = q13.shape[0] // 2
     ab = fp8_gemm(qx, sx, q13, s13)
     h = (silu(ab[:, :I]) * ab[:, I:]).astype(F32)
-    qh, sh = quantize_rows_1x128(h)
+    qh, sh = quantize_rows_1x128(h, ue8m0)
     return fp8_gemm(qh, sh, q2, s2)
 
 
-def layer_forward_fp8(x, topk_idx, topk_gate, wq, shared_wq):
+def layer_forward_fp8(x, topk_idx, topk_gate, wq, shared_wq, ue8m0: bool = False):
     """Expert part of the FP8 layer on the rows of x (bf16 values as fp32).
 
     wq: dict e -> (q13, s13, q2, s2) for the experts that appear in topk_idx;
     shared_wq: list of (q13, s13, q2, s2), one per shared expert. Routing is
-    the same as the bf16 layer's (the router GEMM is not in FP8).
+    the same as the bf16 layer's (the router GEMM is not in FP8). ue8m0
+    selects the power-of-two scale rule for x and h (the weights carry
+    theirs already).
     """
-    qx, sx = quantize_rows_1x128(np.asarray(x, F32))
+    qx, sx = quantize_rows_1x128(np.asarray(x, F32), ue8m0)
     out = np.zeros(np.asarray(x).shape, dtype=F64)  # every expert maps width d back to d
     for (q13, s13, q2, s2) in shared_wq:
-        out += swiglu_ffn_fp8(qx, sx, q13, s13, q2, s2)
+        out += swiglu_ffn_fp8(qx, sx, q13, s13, q2, s2, ue8m0)
     for e in np.unique(topk_idx):
         rows, slots = np.nonzero(topk_idx == e)
-        y = swiglu_ffn_fp8(qx[rows], sx[rows], *wq[int(e)])
+        y = swiglu_ffn_fp8(qx[rows], sx[rows], *wq[int(e)], ue8m0=ue8m0)
         out[rows] += np.asarray(topk_gate, F64)[rows, slots][:, None] * y
     return out
 
 
-def layer_forward_fp8_full(x, w_router, w13, w2, ws13, ws2, bias, G, K, M, group_topk=2):
+def layer_forward_fp8_full(x, w_router, w13, w2, ws13, ws2, bias, G, K, M, group_topk=2,
+                           ue8m0: bool = False):
     """The FP8 layer on the rows of x: bf16-path routing (router_scores,
     select_experts), then 128x128 block quantisation of the master weights of
     every expert the rows use and of the shared experts, then the e4m3 expert
     path of layer_forward_fp8. w13 / w2 / ws13 / ws2 are indexable stacks of
-    per-expert master weights."""
+    per-expert master weights; ue8m0 selects the power-of-two scale rule
+    everywhere."""
     s = router_scores(x, w_router)
     idx, gate = select_experts(s, bias, G, K, M, group_topk)
-    wq = {int(e): quantize_expert_weights(w13[int(e)], w2[int(e)]) for e in np.unique(idx)}
-    shared = [quantize_expert_weights(ws13[i], ws2[i]) for i in range(ws13.shape[0])]
-    out = layer_forward_fp8(np.asarray(x, F32), idx, gate, wq, shared)
+    wq = {int(e): quantize_expert_weights(w13[int(e)], w2[int(e)], ue8m0) for e in np.unique(idx)}
+    shared = [quantize_expert_weights(ws13[i], ws2[i], ue8m0) for i in range(ws13.shape[0])]
+    out = layer_forward_fp8(np.asarray(x, F32), idx, gate, wq, shared, ue8m0)
     return {"scores": s, "topk_idx": idx, "topk_gate": gate, "out": out}

@@ -257,3 +257,137 @@ def test_fp8_layer_without_shared_experts():
     qx, sx = om.quantize_rows_1x128(x)
     want = sum(0.5 * om.swiglu_ffn_fp8(qx, sx, *wq[e]) for e in range(2))
     np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# power-of-two (UE8M0) scale rule
+# --------------------------------------------------------------------------
+
+def _powers_448():
+    return (448.0 * 2.0 ** np.arange(-20, 21)).astype(F32)
+
+
+def test_ue8m0_scale_brute_force():
+    """The scale is the smallest 2^e (e >= -127) with 448 * 2^e >= amax,
+    found here by walking the exponents (exact float64 comparisons)."""
+    rng = np.random.default_rng(21)
+    p = _powers_448()
+    amax = np.concatenate([p, np.nextafter(p, F32(np.inf)), np.nextafter(p, F32(0)),
+                           (rng.uniform(0, 1, 1500) * 10.0 ** rng.integers(-6, 7, 1500)).astype(F32),
+                           np.array([0.0, 1e-40, 3e38], F32)]).astype(F32)
+    sc = om.tile_scale_ue8m0(amax)
+    assert sc.dtype == F32
+    for a, s in zip(amax.tolist(), sc.tolist()):
+        if a == 0.0:
+            assert s == 1.0
+            continue
+        e = next(e for e in range(-127, 128) if 448.0 * 2.0 ** e >= a)
+        assert s == 2.0 ** e, (a, s, e)
+
+
+def _check_pow2_tiles(v_tiles, sc, q_tiles):
+    """Every tile: scale a power of two, amax / scale in (224, 448] (no
+    saturation, no smaller power would do), codes = torch's e4m3 cast of the
+    exact quotient."""
+    import torch
+    for blk, s, q in zip(v_tiles, sc, q_tiles):
+        amax = float(np.abs(blk).max())
+        if amax == 0.0:
+            assert s == 1.0 and not np.any(q)
+            continue
+        m, _ = np.frexp(float(s))
+        assert m == 0.5
+        assert 224.0 < amax / float(s) <= 448.0
+        quot = (blk / s).astype(F32)
+        assert np.array_equal(quot.astype(np.float64) * float(s), blk.astype(np.float64))  # exact division
+        want = torch.from_numpy(quot.copy()).to(torch.float8_e4m3fn).float().numpy()
+        np.testing.assert_array_equal(q, want.astype(np.float64))
+
+
+def test_ue8m0_rows():
+    rng = np.random.default_rng(22)
+    v = (rng.standard_normal((16, 384)) * 10.0 ** rng.uniform(-3, 3, (16, 1))).astype(F32)
+    v[5, 256:] = 0.0
+    q, sc = om.quantize_rows_1x128(v, ue8m0=True)
+    assert sc.shape == (16, 3)
+    tiles = [v[r, b * 128:(b + 1) * 128] for r in range(16) for b in range(3)]
+    qt = [q[r, b * 128:(b + 1) * 128] for r in range(16) for b in range(3)]
+    _check_pow2_tiles(tiles, [sc[r, b] for r in range(16) for b in range(3)], qt)
+
+
+def test_ue8m0_blocks():
+    rng = np.random.default_rng(23)
+    w = (rng.standard_normal((130, 200)) * 0.02).astype(F32)
+    w[:128, 128:] = 0.0
+    q, sc = om.quantize_blocks_128x128(w, ue8m0=True)
+    assert sc.shape == (2, 2)
+    tiles, scs, qt = [], [], []
+    for i in range(2):
+        for j in range(2):
+            tiles.append(w[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128])
+            qt.append(q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128])
+            scs.append(sc[i, j])
+    _check_pow2_tiles(tiles, scs, qt)
+
+
+def test_ue8m0_coincides_with_fp32_rule_on_exact_powers():
+    """When every tile's amax is 448 * 2^k, both scale rules give 2^k, so the
+    two modes quantise identically."""
+    rng = np.random.default_rng(24)
+    v = rng.uniform(-1, 1, (8, 256)).astype(F32)
+    for r in range(8):
+        for b in range(2):
+            v[r, b * 128:(b + 1) * 128] *= F32(2.0 ** (r - b - 3))
+            v[r, b * 128 + (r * 7 + b) % 128] = F32(448.0 * 2.0 ** (r - b - 3)) * (1 if r % 2 else -1)
+    q1, s1 = om.quantize_rows_1x128(v)
+    q2, s2 = om.quantize_rows_1x128(v, ue8m0=True)
+    np.testing.assert_array_equal(s1, s2)
+    np.testing.assert_array_equal(q1, q2)
+
+
+def test_ue8m0_power_of_two_invariance():
+    rng = np.random.default_rng(25)
+    v = rng.standard_normal((4, 256)).astype(F32)
+    q1, s1 = om.quantize_rows_1x128(v, ue8m0=True)
+    q2, s2 = om.quantize_rows_1x128((v * F32(2.0 ** -5)).astype(F32), ue8m0=True)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(s2, s1 * F32(2.0 ** -5))
+
+
+def test_ue8m0_gemm_error_bound():
+    rng = np.random.default_rng(26)
+    a = rng.standard_normal((32, 512)).astype(F32)
+    w = (rng.standard_normal((256, 512)) * 0.006).astype(F32)
+    qa, sa = om.quantize_rows_1x128(a, ue8m0=True)
+    qw, sw = om.quantize_blocks_128x128(w, ue8m0=True)
+    got = om.fp8_gemm(qa, sa, qw, sw)
+    exact = a.astype(np.float64) @ w.astype(np.float64).T
+    # quotients lie in (224, 448] at the tile maximum, so the same 2^-4
+    # relative rounding bound holds, plus the subnormal step of each tile
+    bound = np.abs(a).astype(np.float64) @ np.abs(w).astype(np.float64).T * (2 * 2.0 ** -4 + 2.0 ** -8)
+    assert np.all(np.abs(got - exact) <= bound + 1e-6)
+    assert np.abs(got - exact).max() / np.abs(exact).max() < 0.05
+
+
+def test_ue8m0_layer_differs_only_by_scale_rule():
+    """The UE8M0 FP8 layer stays within the quantisation bound of the exact
+    layer, and its h scales really are the power-of-two ones."""
+    rng = np.random.default_rng(27)
+    T, d, I = 6, 256, 128
+    x = rng.standard_normal((T, d)).astype(F32)
+    w13 = (rng.standard_normal((2, 2 * I, d)) * 0.05).astype(F32)
+    w2 = (rng.standard_normal((2, d, I)) * 0.05).astype(F32)
+    idx = np.array([[0, 1]] * T, np.int32)
+    gate = np.full((T, 2), 0.5, F32)
+    wq = {e: om.quantize_expert_weights(w13[e], w2[e], ue8m0=True) for e in range(2)}
+    for e in range(2):
+        for s in (wq[e][1], wq[e][3]):
+            assert np.all(np.frexp(s.astype(np.float64))[0] == 0.5)
+    out = om.layer_forward_fp8(x, idx, gate, wq, [], ue8m0=True)
+    exact = sum(0.5 * om.swiglu_ffn(x.astype(np.float64), w13[e].astype(np.float64),
+                                    w2[e].astype(np.float64)) for e in range(2))
+    rel = np.abs(out - exact).max() / np.abs(exact).max()
+    assert rel < 0.08
+    out32 = om.layer_forward_fp8(x, idx, gate,
+                                 {e: om.quantize_expert_weights(w13[e], w2[e]) for e in range(2)}, [])
+    assert not np.array_equal(out, out32)
