@@ -63,7 +63,14 @@ typedef enum {
   MOE_ERR_DEVICE = 5        /* device-side check failed (see moe_device_error) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+/* MOE_E4M3: e4m3 codes with fp32 scales, scale = amax / 448 per tile.
+ * MOE_E4M3_UE8M0: e4m3 codes whose tile scales are powers of two, the
+ *   smallest 2^e >= amax / 448 (e in [-127, 127]; 1 for an all-zero tile),
+ *   still passed as fp32 values. The GEMMs then scale inside the tensor
+ *   core (tcgen05 block scaling with UE8M0 scale bytes). The scale rule is
+ *   this library's option beside the pages' fp32 scales [digest-3.1]; only
+ *   the exponent bits of each scale are read. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E4M3_UE8M0 = 3 } moe_dtype;
 
 typedef struct {
   int T, d, E, G, K, M, I, S;
@@ -72,15 +79,16 @@ typedef struct {
                          (2 in DeepSeek-V3 shapes; E/G gives the plain sum
                          over the group's experts, the pages' node score) */
   moe_dtype act;      /* x, out, router weights, yp: MOE_F32 or MOE_BF16 */
-  moe_dtype expert;   /* expert GEMM operands: == act, or MOE_E4M3 with act
-                         MOE_BF16 (1x128 activation tiles, 128x128 weight
-                         blocks, fp32 accumulation [digest-3.1]) */
+  moe_dtype expert;   /* expert GEMM operands: == act, or MOE_E4M3 /
+                         MOE_E4M3_UE8M0 with act MOE_BF16 (1x128 activation
+                         tiles, 128x128 weight blocks, fp32 accumulation
+                         [digest-3.1]) */
 } moe_config;
 
 /* Expert weights. Element type is cfg->expert (router: cfg->act).
  * w13 holds W1 (rows 0..I-1, the gate projection) above W3 (rows I..2I-1,
- * the up projection) for each expert. For MOE_E4M3 each weight matrix carries
- * one fp32 scale per 128x128 block: w = code * scale. */
+ * the up projection) for each expert. For MOE_E4M3 and MOE_E4M3_UE8M0 each
+ * weight matrix carries one fp32 scale per 128x128 block: w = code * scale. */
 typedef struct {
   const void* w_router;      /* [E, d]   act dtype                  */
   const void* w13;           /* [E, 2I, d]                          */
@@ -179,6 +187,12 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
  * to +/-448 [digest-3.1]. Used to prepare MOE_E4M3 expert weights. */
 moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols,
                                      uint8_t* q, float* scale, moe_stream_t stream);
+
+/* The same with power-of-two scales: scale = the smallest 2^e >= amax / 448,
+ * e in [-127, 127] (1 if the block is all zero), code = e4m3(w / scale).
+ * Used to prepare MOE_E4M3_UE8M0 expert weights. */
+moe_status moe_quantize_weights_e4m3_ue8m0(const void* w, int n_mat, int rows, int cols,
+                                           uint8_t* q, float* scale, moe_stream_t stream);
 
 /* Bytes of the fixed device array that moe_permute_static uses as scratch. */
 #define MOE_PERMUTE_STATIC_SCRATCH_BYTES (4u << 20)

@@ -15,8 +15,8 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
 
-MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
-_DT = {"f32": MOE_F32, "bf16": MOE_BF16, "e4m3": MOE_E4M3}
+MOE_F32, MOE_BF16, MOE_E4M3, MOE_E4M3_UE8M0 = 0, 1, 2, 3
+_DT = {"f32": MOE_F32, "bf16": MOE_BF16, "e4m3": MOE_E4M3, "e4m3_ue8m0": MOE_E4M3_UE8M0}
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -57,6 +57,7 @@ _SIGS = {
     "moe_layer_forward": [ctypes.POINTER(moe_config), _P, ctypes.POINTER(moe_weights), _P, ctypes.c_float,
                           _P, _P, _P, _P, _P, _P, _P],
     "moe_quantize_weights_e4m3": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
+    "moe_quantize_weights_e4m3_ue8m0": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
     "moe_permute_static": [ctypes.POINTER(moe_config)] + [_P] * 7 + [_P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_selftest_timeout": [_P, _P],
@@ -161,6 +162,13 @@ def moe_quantize_weights_e4m3(w, q, scale, stream=None):
     """w [n_mat, rows, cols] bf16 -> q uint8 (same shape), scale [n_mat, rows/128, cols/128] fp32."""
     n_mat, rows, cols = w.shape
     _check("moe_quantize_weights_e4m3", lib.moe_quantize_weights_e4m3(
+        _ptr(w), n_mat, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_weights_e4m3_ue8m0(w, q, scale, stream=None):
+    """As moe_quantize_weights_e4m3, with power-of-two (UE8M0) block scales."""
+    n_mat, rows, cols = w.shape
+    _check("moe_quantize_weights_e4m3_ue8m0", lib.moe_quantize_weights_e4m3_ue8m0(
         _ptr(w), n_mat, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
 
 

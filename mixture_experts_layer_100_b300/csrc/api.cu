@@ -32,6 +32,8 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool is_f8(moe_dtype t) { return t == MOE_E4M3 || t == MOE_E4M3_UE8M0; }
+
 // ------------------------------------------------------------ workspace
 struct Layout {
   size_t err, scores, local_rank, chunk_hist, chunk_base, offsets, sorted_tok, slot_pos;
@@ -42,7 +44,7 @@ Layout layout(const moe_config& c) {
   const size_t T = c.T, K = c.K, E = c.E, d = c.d, I = c.I, S = c.S;
   const size_t TK = T * K;
   const size_t nch = (size_t)permute_chunks(c.T);
-  const bool f8 = c.expert == MOE_E4M3;
+  const bool f8 = is_f8(c.expert);
   const size_t ea = elem_bytes(c.act), ex = elem_bytes(c.expert);
   Layout L{};
   size_t o = 0;
@@ -88,12 +90,12 @@ moe_status check_config(const moe_config* c) {
   if (c->K > 32 || c->K > c->M * gsz) return MOE_ERR_INVALID_ARG;
   if (c->E > 512) return MOE_ERR_UNSUPPORTED;
   if (c->act != MOE_F32 && c->act != MOE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->expert != c->act && !(c->expert == MOE_E4M3 && c->act == MOE_BF16)) return MOE_ERR_INVALID_ARG;
+  if (c->expert != c->act && !(is_f8(c->expert) && c->act == MOE_BF16)) return MOE_ERR_INVALID_ARG;
   if ((long long)c->T * c->K > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
   if (c->act == MOE_BF16) {
     if (c->d % 128 != 0 || c->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->E > 256) return MOE_ERR_UNSUPPORTED;
-    if (c->expert == MOE_E4M3 && c->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    if (is_f8(c->expert) && c->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   } else if (c->d % 4 != 0) {
     return MOE_ERR_UNSUPPORTED;
   }
@@ -225,10 +227,11 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
   int* chunk_base = at<int>(ws, Lw.chunk_base);
   MOE_CUDA(launch_permute_rank(topk_idx, c.T, c.K, c.E, local_rank, chunk_hist, err, st));
   MOE_CUDA(launch_permute_scan(counts, chunk_hist, c.T, c.E, chunk_base, offsets, err, st));
-  if (c.expert == MOE_E4M3) {
+  if (is_f8(c.expert)) {
     MOE_CUDA(launch_permute_scatter_e4m3(topk_idx, local_rank, chunk_base, c.T, c.K, c.E,
                                          static_cast<const __nv_bfloat16*>(x), c.d, sorted_tok, slot_pos,
-                                         static_cast<uint8_t*>(xp), xp_scale, xq, xq_scale, num_sms(), st));
+                                         static_cast<uint8_t*>(xp), xp_scale, xq, xq_scale,
+                                         c.expert == MOE_E4M3_UE8M0, num_sms(), st));
   } else {
     MOE_CUDA(launch_permute_scatter(topk_idx, local_rank, chunk_base, c.T, c.K, c.E, x, (size_t)c.d * elem_bytes(c.act),
                                     sorted_tok, slot_pos, xp, num_sms(), st));
@@ -236,7 +239,12 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
   return MOE_OK;
 }
 
-// ---- FP8 expert GEMMs (e4m3 tiles, fp32 promotion per 128-wide K block)
+// ---- FP8 expert GEMMs (e4m3 tiles; fp32 promotion per 128-wide K block, or
+// tensor-core block scaling for power-of-two scales)
+cudaError_t launch_f8(const moe_config& c, const Fp8GemmLaunch& L) {
+  return c.expert == MOE_E4M3_UE8M0 ? launch_mx_gemm(L) : launch_fp8_gemm(L);
+}
+
 moe_status fp8_gemm1(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
                      const uint8_t* xq, const float* xq_scale, const moe_weights* w, bool routed, bool shared,
                      void* ws, cudaStream_t st) {
@@ -287,7 +295,7 @@ moe_status fp8_gemm1(const moe_config& c, const void* xp, const float* xp_scale,
   L.p.err = at<int>(ws, 0);
   L.grid = tc_grid(tiles);
   L.stream = st;
-  MOE_CUDA(launch_fp8_gemm(L));
+  MOE_CUDA(launch_f8(c, L));
   return MOE_OK;
 }
 
@@ -333,7 +341,7 @@ moe_status fp8_gemm2(const moe_config& c, const int32_t* offsets, const moe_weig
   L.p.N = c.d;
   L.p.err = at<int>(ws, 0);
   L.stream = st;
-  MOE_CUDA(launch_fp8_gemm(L));
+  MOE_CUDA(launch_f8(c, L));
   return MOE_OK;
 }
 
@@ -375,7 +383,7 @@ moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scal
     }
     return MOE_OK;
   }
-  if (c.expert == MOE_E4M3) {
+  if (is_f8(c.expert)) {
     return fp8_gemm1(c, xp, xp_scale, offsets, at<uint8_t>(ws, Lw.xq), at<float>(ws, Lw.xq_scale), w, routed,
                      shared, ws, st);
   }
@@ -442,7 +450,7 @@ moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const
     MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(TK, c.E), st));
     return MOE_OK;
   }
-  if (c.expert == MOE_E4M3) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
+  if (is_f8(c.expert)) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kStore;
   L.bn = down_bn(c.d);
@@ -501,7 +509,7 @@ moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_
   // dead once the routed GEMM1 has run), added by the down projection's epilogue
   void* r = at<void>(ws, Lw.xp);
   MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, r, num_sms(), st));
-  if (c.expert == MOE_E4M3) return fp8_gemm2(c, nullptr, w, nullptr, true, r, out, ws, st);
+  if (is_f8(c.expert)) return fp8_gemm2(c, nullptr, w, nullptr, true, r, out, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kCombine;
   L.bn = down_bn(c.d);
@@ -529,7 +537,7 @@ moe_status check_weights(const moe_config& c, const moe_weights* w, bool routed,
   if (routed && (!w->w13 || !w->w2 || !aligned16(w->w13) || !aligned16(w->w2))) return MOE_ERR_INVALID_ARG;
   if (shared && c.S > 0 && (!w->ws13 || !w->ws2 || !aligned16(w->ws13) || !aligned16(w->ws2)))
     return MOE_ERR_INVALID_ARG;
-  if (c.expert == MOE_E4M3) {
+  if (is_f8(c.expert)) {
     if (routed && (!w->w13_scale || !w->w2_scale)) return MOE_ERR_INVALID_ARG;
     if (shared && c.S > 0 && (!w->ws13_scale || !w->ws2_scale)) return MOE_ERR_INVALID_ARG;
   }
@@ -537,6 +545,15 @@ moe_status check_weights(const moe_config& c, const moe_weights* w, bool routed,
 }
 
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+moe_status quantize_weights(const void* w, int n_mat, int rows, int cols, uint8_t* q, float* scale, bool ue8m0,
+                            cudaStream_t st) {
+  if (n_mat < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if (n_mat == 0 || rows == 0 || cols == 0) return MOE_OK;
+  if (!ok_ptr(w) || !ok_ptr(q) || scale == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_quantize_blocks(static_cast<const __nv_bfloat16*>(w), n_mat, rows, cols, q, scale, ue8m0, st));
+  return MOE_OK;
+}
 
 // Side stream of moe_layer_forward (one per host thread and device, created
 // on first use and kept for the life of the process): the shared experts'
@@ -603,7 +620,7 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int
   if (c.T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(counts) || !ok_ptr(sorted_tok) || !ok_ptr(slot_pos) || !ok_ptr(x) ||
                   !ok_ptr(xp)))
     return MOE_ERR_INVALID_ARG;
-  if (c.expert == MOE_E4M3 && c.T > 0 && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_f8(c.expert) && c.T > 0 && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
   return permute_stage(c, topk_idx, counts, offsets, sorted_tok, slot_pos, x, xp, xp_scale, nullptr, nullptr, ws,
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -616,7 +633,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const float* x
   if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
   if (c.T == 0) return MOE_OK;
   if (!ok_ptr(xp) || !ok_ptr(offsets) || !ok_ptr(yp)) return MOE_ERR_INVALID_ARG;
-  if (c.expert == MOE_E4M3 && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_f8(c.expert) && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   MOE_TRY(gemm1_stage(c, xp, xp_scale, offsets, nullptr, w, true, false, ws, st));
   MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
@@ -634,10 +651,10 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
   if (c.S > 0 && !ok_ptr(x)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (c.S > 0) {
-    if (c.expert == MOE_E4M3) {
+    if (is_f8(c.expert)) {
       const Layout Lw = layout(c);
       MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
-                                    at<float>(ws, Lw.xq_scale), num_sms(), st));
+                                    at<float>(ws, Lw.xq_scale), c.expert == MOE_E4M3_UE8M0, num_sms(), st));
     }
     MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, st));
   }
@@ -672,7 +689,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
   MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
   if (c.T > 0) {
     float* scores = at<float>(ws, Lw.scores);
-    const bool f8 = c.expert == MOE_E4M3;
+    const bool f8 = is_f8(c.expert);
     MOE_TRY(router_scores(c, x, w->w_router, scores, ws, st));
     MOE_TRY(stage_mark(1, st));
     // The shared experts' GEMM1 depends on x only: it runs on a side stream,
@@ -685,7 +702,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
       MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
       if (f8) {
         MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
-                                      at<float>(ws, Lw.xq_scale), num_sms(), side->s));
+                                      at<float>(ws, Lw.xq_scale), c.expert == MOE_E4M3_UE8M0, num_sms(),
+                                      side->s));
       }
       MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, side->s));
       MOE_CUDA(cudaEventRecord(side->join, side->s));
@@ -716,12 +734,12 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
 
 moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols, uint8_t* q, float* scale,
                                      moe_stream_t stream) {
-  if (n_mat < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
-  if (n_mat == 0 || rows == 0 || cols == 0) return MOE_OK;
-  if (!ok_ptr(w) || !ok_ptr(q) || scale == nullptr) return MOE_ERR_INVALID_ARG;
-  MOE_CUDA(launch_quantize_blocks(static_cast<const __nv_bfloat16*>(w), n_mat, rows, cols, q, scale,
-                                  reinterpret_cast<cudaStream_t>(stream)));
-  return MOE_OK;
+  return quantize_weights(w, n_mat, rows, cols, q, scale, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_quantize_weights_e4m3_ue8m0(const void* w, int n_mat, int rows, int cols, uint8_t* q, float* scale,
+                                           moe_stream_t stream) {
+  return quantize_weights(w, n_mat, rows, cols, q, scale, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_set_stage_events(void* const* events, int count) {

@@ -36,9 +36,11 @@ __global__ void __launch_bounds__(512) bias_update_kernel(const int* __restrict_
 }
 
 // 128 x 128 block quantisation of bf16 matrices [n_mat, rows, cols]. One
-// block of 256 threads per 128 x 128 tile; each thread owns half a row.
+// block of 256 threads per 128 x 128 tile; each thread owns half a row. The
+// scale follows e4m3_tile_scale (fp32 or UE8M0 rule).
 __global__ void __launch_bounds__(256) quantize_blocks_kernel(const __nv_bfloat16* __restrict__ w, int rows, int cols,
-                                                              uint8_t* __restrict__ q, float* __restrict__ scale) {
+                                                              uint8_t* __restrict__ q, float* __restrict__ scale,
+                                                              bool ue8m0) {
   const int bc = blockIdx.x, br = blockIdx.y, mat = blockIdx.z;
   const int nbr = gridDim.y, nbc = gridDim.x;
   const int r = br * 128 + (threadIdx.x >> 1);
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(const __nv_bfloat1
   float m = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
-  const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+  const float s = e4m3_tile_scale(m, ue8m0);
   if (threadIdx.x == 0) scale[((size_t)mat * nbr + br) * nbc + bc] = s;
   if (r < rows) {
     uint8_t* dst = q + (size_t)mat * rows * cols;
@@ -73,9 +75,10 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(const __nv_bfloat1
 // 1 x 128 tiles of a bf16 activation matrix [rows, d] (d % 128 == 0): codes
 // [rows, d], scales tile-major [d/128, rows]. Each warp takes two tiles per
 // step, one per half-warp; the loop is uniform across the warp so that the
-// shuffles always see all 32 lanes.
+// shuffles always see all 32 lanes. The scale follows e4m3_tile_scale.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int rows, int d,
-                                                            uint8_t* __restrict__ q, float* __restrict__ scale) {
+                                                            uint8_t* __restrict__ q, float* __restrict__ scale,
+                                                            bool ue8m0) {
   const int ntiles = d / 128;
   const long long total = (long long)rows * ntiles;
   const int lane = threadIdx.x & 31;
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (!act) continue;
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float s = e4m3_tile_scale(amax, ue8m0);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], s)) << (8 * j);
@@ -120,17 +123,17 @@ cudaError_t launch_bias_update(const int* counts, int E, long long TK, float gam
 }
 
 cudaError_t launch_quantize_blocks(const __nv_bfloat16* w, int n_mat, int rows, int cols, uint8_t* q, float* scale,
-                                   cudaStream_t st) {
+                                   bool ue8m0, cudaStream_t st) {
   dim3 grid((cols + 127) / 128, (rows + 127) / 128, n_mat);
-  quantize_blocks_kernel<<<grid, 256, 0, st>>>(w, rows, cols, q, scale);
+  quantize_blocks_kernel<<<grid, 256, 0, st>>>(w, rows, cols, q, scale, ue8m0);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_rows(const __nv_bfloat16* x, int rows, int d, uint8_t* q, float* scale, int num_sms,
-                                 cudaStream_t st) {
+cudaError_t launch_quantize_rows(const __nv_bfloat16* x, int rows, int d, uint8_t* q, float* scale, bool ue8m0,
+                                 int num_sms, cudaStream_t st) {
   const long long warps = ((long long)rows * (d / 128) + 1) / 2;
   const long long blocks = std::max(1LL, std::min((warps * 32 + 255) / 256, (long long)num_sms * 16));
-  quantize_rows_kernel<<<(int)blocks, 256, 0, st>>>(x, rows, d, q, scale);
+  quantize_rows_kernel<<<(int)blocks, 256, 0, st>>>(x, rows, d, q, scale, ue8m0);
   return cudaGetLastError();
 }
 

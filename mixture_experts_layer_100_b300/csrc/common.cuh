@@ -40,6 +40,26 @@ __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat1
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Scale of one e4m3 tile whose largest magnitude is amax; 1 for an all-zero
+// tile. The fp32 rule is amax / 448. The UE8M0 rule is the smallest power of
+// two 2^e >= amax / 448 with e clamped to [-127, 127] (the exponents a UE8M0
+// byte holds), read off the bits of amax: amax = 1.f * 2^(x - 127) and
+// 448 = 1.75 * 2^8, so 2^(x - 135) is the answer unless 1.f > 1.75, when it
+// is twice that. 2^-127 is returned as the fp32 subnormal 0x00400000.
+__device__ __forceinline__ float e4m3_tile_scale(float amax, bool ue8m0) {
+  if (!(amax > 0.0f)) return 1.0f;
+  if (!ue8m0) return __fdiv_rn(amax, 448.0f);
+  const uint32_t b = __float_as_uint(amax);
+  const int x = (int)(b >> 23);
+  int e = x == 0 ? -127 : x - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = max(-127, min(127, e));
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// UE8M0 byte (biased exponent, 2^-127 -> 0) of a positive power-of-two scale.
+// The mantissa bits of any other value are ignored.
+__device__ __forceinline__ uint32_t ue8m0_byte(float s) { return (__float_as_uint(s) >> 23) & 0xFFu; }
+
 // e4m3 code of v (round to nearest even, saturating to +/-448).
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
   return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);

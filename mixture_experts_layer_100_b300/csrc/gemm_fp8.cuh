@@ -1,5 +1,6 @@
-// FP8 (e4m3) grouped GEMM on tcgen05 with 1x128 / 128x128 scales and fp32
-// promotion of every 128-wide K block (see gemm_fp8.cu).
+// FP8 (e4m3) grouped GEMMs on tcgen05 with 1x128 / 128x128 scales: fp32
+// promotion of every 128-wide K block (gemm_fp8.cu), or tensor-core block
+// scaling for power-of-two scales (gemm_mx.cu).
 #pragma once
 
 #include <cuda.h>
@@ -45,5 +46,9 @@ struct Fp8GemmLaunch {
 };
 
 cudaError_t launch_fp8_gemm(const Fp8GemmLaunch& L);
+
+// Same operands and epilogues with power-of-two scales, scaled inside the
+// tensor core (gemm_mx.cu).
+cudaError_t launch_mx_gemm(const Fp8GemmLaunch& L);
 
 }  // namespace moe

@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 // Same positions; each token row (bf16) is cut into 1x128 tiles and written
 // to its K places as e4m3 codes, with one fp32 scale per tile:
-// scale = amax / 448 (1 for an all-zero tile), code = e4m3(v / scale).
+// scale = e4m3_tile_scale(amax) (amax / 448, or the UE8M0 power of two; 1 for
+// an all-zero tile), code = e4m3(v / scale).
 // A half-warp covers one 128-element tile (8 elements per lane). When xq is
 // given, the quantised row is also written once in token order (for the
 // shared experts). Scales are stored tile-major: scale[tile * rows + row].
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                                 const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
                                 const __nv_bfloat16* __restrict__ x, int d, int* __restrict__ sorted_tok,
                                 int* __restrict__ slot_pos, uint8_t* __restrict__ xp, float* __restrict__ xp_scale,
-                                uint8_t* __restrict__ xq, float* __restrict__ xq_scale) {
+                                uint8_t* __restrict__ xq, float* __restrict__ xq_scale, bool ue8m0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = d / 128;
   const int TK = T * K;
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      const float scale = e4m3_tile_scale(amax, ue8m0);
       uint2 packed = make_uint2(0, 0);
       if (act) {
         uint32_t lo = 0, hi = 0;
@@ -230,12 +231,13 @@ cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, c
 
 cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
                                         int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
-                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, int num_sms,
-                                        cudaStream_t st) {
+                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, bool ue8m0,
+                                        int num_sms, cudaStream_t st) {
   const int nchunks = permute_chunks(T);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
   permute_scatter_e4m3_kernel<<<blocks, kWarps * 32, 0, st>>>(topk_idx, local_rank, chunk_base, T, K, E, nchunks, x,
-                                                              d, sorted_tok, slot_pos, xp, xp_scale, xq, xq_scale);
+                                                              d, sorted_tok, slot_pos, xp, xp_scale, xq, xq_scale,
+                                                              ue8m0);
   return cudaGetLastError();
 }
 

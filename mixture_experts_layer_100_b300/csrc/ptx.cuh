@@ -154,6 +154,41 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// D[tmem] (+)= (A . scale_A)(B . scale_B)^T for e4m3 inputs with one UE8M0
+// scale per 32 K values of every A and B row (kind::mxf8f6f4, block_scale,
+// scale_vec::1X). The scales are read from TMEM: A row i from lane i, column
+// sfa + i/32; B row j (for accumulator row i) from lane 32*(i/32) + j%32,
+// column sfb + j/32; in both the byte named by the descriptor's scale id
+// (0 here). This layout was measured on sm_103a.
+__device__ __forceinline__ void mma_mx_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Asynchronous copy of 32 rows of 16 bytes from shared memory into TMEM,
+// repeated in all four lane quarters: word c of row l lands in lane 32q + l,
+// column taddr + c, for q = 0..3. Ordered before later tcgen05.mma of the
+// same thread; tracked by tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Shared-memory descriptor of a block of 16-byte rows without swizzle: 8-row
+// core matrices of 128 contiguous bytes, the next 8 rows 128 bytes further.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                     // leading byte offset (one 16-byte column: unused)
+  d |= (uint64_t)(128 >> 4) << 32;            // stride byte offset
+  d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+  return d;                                   // swizzle mode 0: none
+}
+
 // Instruction descriptor (kind::f16 / kind::f8f6f4, dense, fp32 D, both
 // operands K-major): D format at bits 4-5, A/B formats at 7-9 / 10-12,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -162,6 +197,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: e4m3 A and B
+// (format 0 at bits 7-9 / 10-12), K-major, N >> 3 at bits 17-22, UE8M0
+// scales (bit 23), M >> 4 at bits 24-28; scale ids (bits 4-5 for B, 29-30 for
+// A) 0. D is always fp32.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA

@@ -48,7 +48,7 @@ class Preset:
     I: int            # expert intermediate width
     S: int            # shared experts
     dtype: str        # "f32" or "bf16": activations, master weights, output
-    expert_dtype: str  # "f32", "bf16" or "e4m3": expert GEMM operands
+    expert_dtype: str  # "f32", "bf16", "e4m3" or "e4m3_ue8m0" (power-of-two scales): expert GEMM operands
     bias: str         # "zeros", "u0.01" or "u0.02"
     zipf: bool        # add the rank-8 routing-skew component to x
     steps: int        # forward + bias-update steps the workload runs
@@ -80,6 +80,10 @@ PRESETS = {
                zipf=False, steps=1),
         Preset("v3_t32768_d7168_e256_fp8", T=32768, d=7168, E=256, G=8, K=8,
                M=4, I=2048, S=1, dtype="bf16", expert_dtype="e4m3",
+               bias="zeros", zipf=True, steps=50),
+        # the same workload with power-of-two (UE8M0) tile scales
+        Preset("v3_t32768_d7168_e256_fp8_ue8m0", T=32768, d=7168, E=256, G=8, K=8,
+               M=4, I=2048, S=1, dtype="bf16", expert_dtype="e4m3_ue8m0",
                bias="zeros", zipf=True, steps=50),
     ]
 }

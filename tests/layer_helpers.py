@@ -9,7 +9,7 @@ from mixture_experts_layer_100_b300 import synth
 from oracle import moe_oracle as om
 
 DEV = "cuda"
-TOL = {"f32": 1e-5, "bf16": 2e-2, "e4m3": 6e-2}
+TOL = {"f32": 1e-5, "bf16": 2e-2, "e4m3": 6e-2, "e4m3_ue8m0": 6e-2}
 
 
 class LazyStack:
@@ -91,17 +91,19 @@ def compare(p, res, ref, bias, tokens=None, dtype=None, max_flip=0.01):
     return err, int((~same).sum())
 
 
-def quantize_device_weights(wd: dict) -> dict:
+def quantize_device_weights(wd: dict, ue8m0: bool = False) -> dict:
     """e4m3 codes + 128x128 block scales of the expert weights, made on the
-    GPU by moe_quantize_weights_e4m3 (the router stays in the master dtype)."""
+    GPU by moe_quantize_weights_e4m3 (or its power-of-two variant); the
+    router stays in the master dtype."""
     from mixture_experts_layer_100_b300 import binding as B
+    quant = B.moe_quantize_weights_e4m3_ue8m0 if ue8m0 else B.moe_quantize_weights_e4m3
     out = {"w_router": wd["w_router"]}
     for k in ("w13", "w2", "ws13", "ws2"):
         w = wd[k]
         n, r, c = w.shape
         q = torch.empty((n, r, c), dtype=torch.uint8, device=DEV)
         sc = torch.empty((n, (r + 127) // 128, (c + 127) // 128), dtype=torch.float32, device=DEV)
-        B.moe_quantize_weights_e4m3(w, q, sc)
+        quant(w, q, sc)
         out[k] = q
         out[k + "_scale"] = sc
     torch.cuda.synchronize()
@@ -109,9 +111,11 @@ def quantize_device_weights(wd: dict) -> dict:
 
 
 def oracle_rows_fp8(p, w: synth.Weights, x: torch.Tensor, b: torch.Tensor, tokens=None):
-    """FP8 oracle layer output for the given tokens (all when None)."""
+    """FP8 oracle layer output for the given tokens (all when None), with the
+    preset's scale rule."""
     xs = x if tokens is None else x[torch.as_tensor(tokens)]
     lazy = w.w13.is_cuda
     W = (lambda t: LazyStack(t)) if lazy else (lambda t: t.double().numpy())
     return om.layer_forward_fp8_full(host(xs).astype(np.float64), host(w.w_router), W(w.w13), W(w.w2),
-                                     W(w.ws13), W(w.ws2), b.cpu().numpy(), p.G, p.K, p.M, p.group_topk)
+                                     W(w.ws13), W(w.ws2), b.cpu().numpy(), p.G, p.K, p.M, p.group_topk,
+                                     ue8m0=p.expert_dtype == "e4m3_ue8m0")
