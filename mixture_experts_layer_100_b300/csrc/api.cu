@@ -37,7 +37,7 @@ bool is_f8(moe_dtype t) { return t == MOE_E4M3 || t == MOE_E4M3_UE8M0; }
 // ------------------------------------------------------------ workspace
 struct Layout {
   size_t err, scores, local_rank, chunk_hist, chunk_base, offsets, sorted_tok, slot_pos;
-  size_t xp, xp_scale, xq, xq_scale, h, h_scale, hs, hs_scale, yp, total;
+  size_t xp, xp_scale, xq, xq_scale, tok_scale, h, h_scale, hs, hs_scale, yp, total;
 };
 
 Layout layout(const moe_config& c) {
@@ -65,6 +65,7 @@ Layout layout(const moe_config& c) {
   L.xp_scale = take(f8 ? (d / 128) * TK * 4 : 0);
   L.xq = take(f8 ? T * d : 0);
   L.xq_scale = take(f8 ? (d / 128) * T * 4 : 0);
+  L.tok_scale = take(f8 ? (d / 128) * T * 4 : 0);
   L.h = take(TK * I * ex);
   L.h_scale = take(f8 ? (I / 128) * TK * 4 : 0);
   L.hs = take(T * S * I * ex);
@@ -231,7 +232,7 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
     MOE_CUDA(launch_permute_scatter_e4m3(topk_idx, local_rank, chunk_base, c.T, c.K, c.E,
                                          static_cast<const __nv_bfloat16*>(x), c.d, sorted_tok, slot_pos,
                                          static_cast<uint8_t*>(xp), xp_scale, xq, xq_scale,
-                                         c.expert == MOE_E4M3_UE8M0, num_sms(), st));
+                                         at<float>(ws, Lw.tok_scale), c.expert == MOE_E4M3_UE8M0, num_sms(), st));
   } else {
     MOE_CUDA(launch_permute_scatter(topk_idx, local_rank, chunk_base, c.T, c.K, c.E, x, (size_t)c.d * elem_bytes(c.act),
                                     sorted_tok, slot_pos, xp, num_sms(), st));

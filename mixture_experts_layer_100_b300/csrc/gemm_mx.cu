@@ -43,8 +43,9 @@ constexpr int kStageX = kABytesX + kBBytesX;
 constexpr int kSfaBytes = 512;   // 128 A rows, one word each (4 copies of the byte)
 constexpr int kSfbBytes = 1024;  // 256 B rows
 constexpr int kSfBytes = kSfaBytes + kSfbBytes;
-constexpr int kAuxX = 12288;
-constexpr int kSmemX = 1024 + kStagesX * (kStageX + kSfBytes) + kAuxX;
+constexpr int kAuxX = 8192;
+constexpr int kStgWarp = 2048;    // per epilogue warp: 32 rows x 64 bytes of bf16 output
+constexpr int kSmemX = 1024 + kStagesX * (kStageX + kSfBytes) + kAuxX + 8 * kStgWarp;
 constexpr uint32_t kSfCol = 256;  // first TMEM column of the scale slots
 constexpr uint32_t kSfSlot = 16;  // TMEM columns per slot
 
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
   int* s_mt = s_tp + (kMaxGroups + 1);
   int* s_off = s_mt + kMaxGroups;
   float* s_amax = reinterpret_cast<float*>(s_off + kMaxGroups + 1);  // [2][128]
+  uint8_t* s_stage_out = aux + kAuxX;                                 // [8 warps][2048]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -423,35 +425,83 @@ __global__ void __launch_bounds__(kThreadsX, 1)
         epi_bar_x();  // s_amax is rewritten by the next tile
         const float scale = e4m3_tile_scale(amax, true);
         const float inv = __fdiv_rn(1.0f, scale);  // exact: scale is a power of two
-        if (valid && ok) {
+        // the row's 64 codes go through the warp's staging block (layout as
+        // in the bf16 store below), then out as 8 rows x 64 bytes per store
+        uint8_t* stg = s_stage_out + (warp - 3) * kStgWarp;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float* a = acc + 16 * v;
+          uint4 w;
+          w.x = pack4_e4m3_x(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+          w.y = pack4_e4m3_x(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
+          w.z = pack4_e4m3_x(a[8] * inv, a[9] * inv, a[10] * inv, a[11] * inv);
+          w.w = pack4_e4m3_x(a[12] * inv, a[13] * inv, a[14] * inv, a[15] * inv);
+          *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
+        }
+        __syncwarp();
+        {
           uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
           const int ldo = t.seg ? p.ldo1 : p.ldo0;
-          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + half * 64);
+          const int rbase = t.row0 + 32 * q;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float* a = acc + 16 * v;
-            uint4 w;
-            w.x = pack4_e4m3_x(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
-            w.y = pack4_e4m3_x(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
-            w.z = pack4_e4m3_x(a[8] * inv, a[9] * inv, a[10] * inv, a[11] * inv);
-            w.w = pack4_e4m3_x(a[12] * inv, a[13] * inv, a[14] * inv, a[15] * inv);
-            dst[v] = w;
-          }
-          if (half == 0) {
-            float* hs = t.seg ? p.out_scale1 : p.out_scale0;
-            hs[(size_t)t.n * rows_total + row] = scale;
+          for (int k = 0; k < 4; ++k) {
+            const int r = 8 * k + (lane >> 2), j = lane & 3;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+            if (ok && rbase + r < t.row_end)
+              *reinterpret_cast<uint4*>(out + (size_t)(rbase + r) * ldo + t.n * 128 + half * 64 + 16 * j) = w;
           }
         }
-      } else {
+        __syncwarp();
+        if (valid && ok && half == 0) {
+          float* hs = t.seg ? p.out_scale1 : p.out_scale0;
+          hs[(size_t)t.n * rows_total + row] = scale;
+        }
+      } else if constexpr (EPI == Fp8Epi::kCombine) {
         if (valid && ok) {
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
           const int ldo = t.seg ? p.ldo1 : p.ldo0;
           const size_t o = (size_t)row * ldo + t.n * kBNx + half * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
+            add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
             store_bf16x32(out + o + 32 * c, acc + 32 * c);
           }
+        }
+      } else {
+        // bf16 rows through a per-warp staging block, so that each store
+        // instruction writes 8 rows x 64 contiguous bytes instead of 32 rows
+        // x 16 bytes. Staging layout: row r, 16-byte chunk j at
+        // r * 64 + (j ^ ((r >> 1) & 3)) * 16 (conflict-free both ways).
+        uint8_t* stg = s_stage_out + (warp - 3) * kStgWarp;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
+        const int ldo = t.seg ? p.ldo1 : p.ldo0;
+        const int col0 = t.n * kBNx + half * 128;
+        const int rbase = t.row0 + 32 * q;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float* a = acc + 32 * c + 8 * j;
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(a[4], a[5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(a[6], a[7]);
+            w.x = *reinterpret_cast<uint32_t*>(&h0);
+            w.y = *reinterpret_cast<uint32_t*>(&h1);
+            w.z = *reinterpret_cast<uint32_t*>(&h2);
+            w.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = w;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = 8 * k + (lane >> 2), j = lane & 3;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+            if (ok && rbase + r < t.row_end)
+              *reinterpret_cast<uint4*>(out + (size_t)(rbase + r) * ldo + col0 + 32 * c + 8 * j) = w;
+          }
+          __syncwarp();
         }
       }
     }

@@ -25,8 +25,8 @@ cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, c
                                    int num_sms, cudaStream_t st);
 cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
                                         int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
-                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, bool ue8m0,
-                                        int num_sms, cudaStream_t st);
+                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, float* tok_scale,
+                                        bool ue8m0, int num_sms, cudaStream_t st);
 
 // ---- bias update and quantisers (bias_quant.cu)
 cudaError_t launch_bias_update(const int* counts, int E, long long TK, float gamma, float* bias,

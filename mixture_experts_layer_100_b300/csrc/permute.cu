@@ -125,16 +125,18 @@ __global__ void __launch_bounds__(kWarps * 32)
 // an all-zero tile), code = e4m3(v / scale).
 // A half-warp covers one 128-element tile (8 elements per lane). When xq is
 // given, the quantised row is also written once in token order (for the
-// shared experts). Scales are stored tile-major: scale[tile * rows + row].
+// shared experts). The scales go out once per token, token-major
+// (tok_scale[t * ntiles + tile]); scale_tiles_kernel then lays them out
+// tile-major for the permuted rows, which keeps this kernel's writes whole
+// sectors instead of one 4-byte store per (token, copy, tile).
 __global__ void __launch_bounds__(kWarps * 32)
     permute_scatter_e4m3_kernel(const int* __restrict__ topk_idx, const int* __restrict__ local_rank,
                                 const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
                                 const __nv_bfloat16* __restrict__ x, int d, int* __restrict__ sorted_tok,
-                                int* __restrict__ slot_pos, uint8_t* __restrict__ xp, float* __restrict__ xp_scale,
-                                uint8_t* __restrict__ xq, float* __restrict__ xq_scale, bool ue8m0) {
+                                int* __restrict__ slot_pos, uint8_t* __restrict__ xp, float* __restrict__ tok_scale,
+                                uint8_t* __restrict__ xq, bool ue8m0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = d / 128;
-  const int TK = T * K;
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     int pos = -1;
     if (lane < K) {
@@ -178,15 +180,33 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
       for (int k = 0; k < K; ++k) {
         const int pk = __shfl_sync(0xffffffffu, pos, k);
-        if (act && pk >= 0) {
-          reinterpret_cast<uint2*>(xp + (size_t)pk * d + tile * 128)[lane & 15] = packed;
-          if ((lane & 15) == 0) xp_scale[(size_t)tile * TK + pk] = scale;
-        }
+        if (act && pk >= 0) reinterpret_cast<uint2*>(xp + (size_t)pk * d + tile * 128)[lane & 15] = packed;
       }
-      if (act && xq != nullptr) {
-        reinterpret_cast<uint2*>(xq + (size_t)t * d + tile * 128)[lane & 15] = packed;
-        if ((lane & 15) == 0) xq_scale[(size_t)tile * T + t] = scale;
-      }
+      if (act && (lane & 15) == 0) tok_scale[(size_t)t * ntiles + tile] = scale;
+      if (act && xq != nullptr) reinterpret_cast<uint2*>(xq + (size_t)t * d + tile * 128)[lane & 15] = packed;
+    }
+  }
+}
+
+// Tile-major scales of the permuted rows, xp_scale[tile * TK + pos] =
+// tok_scale[sorted_tok[pos] * ntiles + tile], and (when xq_scale is given)
+// of the token-order rows, xq_scale[tile * T + t] = tok_scale[t * ntiles +
+// tile]: coalesced writes, gathered reads of the small token-major table.
+__global__ void __launch_bounds__(256)
+    scale_tiles_kernel(const float* __restrict__ tok_scale, const int* __restrict__ sorted_tok, int T, int TK,
+                       int ntiles, float* __restrict__ xp_scale, float* __restrict__ xq_scale) {
+  const long long n_p = (long long)ntiles * TK;
+  const long long n_q = xq_scale != nullptr ? (long long)ntiles * T : 0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_p + n_q; i += stride) {
+    if (i < n_p) {
+      const int tile = (int)(i / TK), pos = (int)(i % TK);
+      const int t = sorted_tok[pos];
+      xp_scale[i] = (t >= 0 && t < T) ? tok_scale[(size_t)t * ntiles + tile] : 1.0f;
+    } else {
+      const long long j = i - n_p;
+      const int tile = (int)(j / T), t = (int)(j % T);
+      xq_scale[j] = tok_scale[(size_t)t * ntiles + tile];
     }
   }
 }
@@ -231,13 +251,18 @@ cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, c
 
 cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
                                         int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
-                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, bool ue8m0,
-                                        int num_sms, cudaStream_t st) {
+                                        uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, float* tok_scale,
+                                        bool ue8m0, int num_sms, cudaStream_t st) {
   const int nchunks = permute_chunks(T);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
   permute_scatter_e4m3_kernel<<<blocks, kWarps * 32, 0, st>>>(topk_idx, local_rank, chunk_base, T, K, E, nchunks, x,
-                                                              d, sorted_tok, slot_pos, xp, xp_scale, xq, xq_scale,
-                                                              ue8m0);
+                                                              d, sorted_tok, slot_pos, xp, tok_scale, xq, ue8m0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int ntiles = d / 128;
+  const long long n = (long long)ntiles * ((long long)T * K + (xq_scale != nullptr ? T : 0));
+  const int sblocks = (int)std::max(1LL, std::min((n + 255) / 256, (long long)num_sms * 8));
+  scale_tiles_kernel<<<sblocks, 256, 0, st>>>(tok_scale, sorted_tok, T, T * K, ntiles, xp_scale, xq_scale);
   return cudaGetLastError();
 }
 
