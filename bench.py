@@ -140,10 +140,17 @@ def dist_env():
     return world, rank, local
 
 
-TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_epi.cuh", "gemm_sched.cuh", "api.cu")
+# kernel and launch sources that the roofline kernel's recorded DRAM traffic
+# depends on, per expert-GEMM dtype (profiles/traffic.json, key
+# "gemm1_swiglu:<dtype>")
+TRAFFIC_SOURCES = {
+    "bf16": ("gemm_tc.cu", "gemm_epi.cuh", "gemm_sched.cuh", "api.cu"),
+    "e4m3": ("gemm_fp8.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "api.cu"),
+    "e4m3_ue8m0": ("gemm_mx.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "api.cu"),
+}
 
 
-def source_sha(files=TRAFFIC_SOURCES) -> str:
+def source_sha(files) -> str:
     """Hash of the kernel and launch sources a traffic measurement depends on."""
     h = hashlib.sha256()
     for f in files:
@@ -152,13 +159,15 @@ def source_sha(files=TRAFFIC_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(key: str):
-    """DRAM bytes per launch recorded in profiles/ for the current kernel and
-    launch sources (None when either changed since the capture)."""
+def traffic_from_profiles(stage: str, dtype: str):
+    """DRAM bytes per launch recorded in profiles/ for this stage's kernel at
+    the given expert dtype, if its kernel and launch sources are unchanged
+    since the capture (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[key]
-        return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha() else None
+            rec = json.load(f)[f"{stage}:{dtype}"]
+        ok = rec.get("source_sha") == source_sha(TRAFFIC_SOURCES[dtype])
+        return rec["bytes_per_launch"] if ok else None
     except Exception:
         return None
 
@@ -426,7 +435,7 @@ def run_ours(a, p):
                 "achieved": g1, "peak": tf_sust, "unit": "TFLOP/s", "frac": g1 / tf_sust,
                 "peak_kind": f"{'fp8' if f8 else 'bf16'} dense, sustained ({src})",
                 "frac_of_burst_peak": g1 / tf_burst,
-                "traffic": traffic_from_profiles("gemm1_swiglu")}
+                "traffic": traffic_from_profiles("gemm1_swiglu", p.expert_dtype)}
     stages = {}
     hb = hbm_bytes(p)
     for name in STAGES:
