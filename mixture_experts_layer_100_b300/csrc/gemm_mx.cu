@@ -44,7 +44,7 @@ constexpr int kSfaBytes = 512;   // 128 A rows, one word each (4 copies of the b
 constexpr int kSfbBytes = 1024;  // 256 B rows
 constexpr int kSfBytes = kSfaBytes + kSfbBytes;
 constexpr int kAuxX = 8192;
-constexpr int kStgWarp = 2048;    // per epilogue warp: 32 rows x 64 bytes of bf16 output
+constexpr int kStgWarp = kRowStageBytes;  // per epilogue warp: 32 rows x 64 bytes of output
 constexpr int kSmemX = 1024 + kStagesX * (kStageX + kSfBytes) + kAuxX + 8 * kStgWarp;
 constexpr uint32_t kSfCol = 256;  // first TMEM column of the scale slots
 constexpr uint32_t kSfSlot = 16;  // TMEM columns per slot
@@ -425,33 +425,24 @@ __global__ void __launch_bounds__(kThreadsX, 1)
         epi_bar_x();  // s_amax is rewritten by the next tile
         const float scale = e4m3_tile_scale(amax, true);
         const float inv = __fdiv_rn(1.0f, scale);  // exact: scale is a power of two
-        // the row's 64 codes go through the warp's staging block (layout as
-        // in the bf16 store below), then out as 8 rows x 64 bytes per store
-        uint8_t* stg = s_stage_out + (warp - 3) * kStgWarp;
+        // the row's 64 codes, out through the warp's staging block
+        uint4 w[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const float* a = acc + 16 * v;
-          uint4 w;
-          w.x = pack4_e4m3_x(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
-          w.y = pack4_e4m3_x(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
-          w.z = pack4_e4m3_x(a[8] * inv, a[9] * inv, a[10] * inv, a[11] * inv);
-          w.w = pack4_e4m3_x(a[12] * inv, a[13] * inv, a[14] * inv, a[15] * inv);
-          *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
+          w[v].x = pack4_e4m3_x(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+          w[v].y = pack4_e4m3_x(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
+          w[v].z = pack4_e4m3_x(a[8] * inv, a[9] * inv, a[10] * inv, a[11] * inv);
+          w[v].w = pack4_e4m3_x(a[12] * inv, a[13] * inv, a[14] * inv, a[15] * inv);
         }
-        __syncwarp();
         {
           uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
           const int ldo = t.seg ? p.ldo1 : p.ldo0;
           const int rbase = t.row0 + 32 * q;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = 8 * k + (lane >> 2), j = lane & 3;
-            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
-            if (ok && rbase + r < t.row_end)
-              *reinterpret_cast<uint4*>(out + (size_t)(rbase + r) * ldo + t.n * 128 + half * 64 + 16 * j) = w;
-          }
+          const int nrows = ok ? max(0, min(32, t.row_end - rbase)) : 0;
+          warp_store_rows64(s_stage_out + (warp - 3) * kStgWarp, lane, w,
+                            out + (size_t)rbase * ldo + t.n * 128 + half * 64, (size_t)ldo, nrows);
         }
-        __syncwarp();
         if (valid && ok && half == 0) {
           float* hs = t.seg ? p.out_scale1 : p.out_scale0;
           hs[(size_t)t.n * rows_total + row] = scale;
@@ -468,40 +459,18 @@ __global__ void __launch_bounds__(kThreadsX, 1)
           }
         }
       } else {
-        // bf16 rows through a per-warp staging block, so that each store
-        // instruction writes 8 rows x 64 contiguous bytes instead of 32 rows
-        // x 16 bytes. Staging layout: row r, 16-byte chunk j at
-        // r * 64 + (j ^ ((r >> 1) & 3)) * 16 (conflict-free both ways).
-        uint8_t* stg = s_stage_out + (warp - 3) * kStgWarp;
+        // bf16 rows, 32 columns at a time through the warp's staging block
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
         const int ldo = t.seg ? p.ldo1 : p.ldo0;
-        const int col0 = t.n * kBNx + half * 128;
         const int rbase = t.row0 + 32 * q;
+        const int nrows = ok ? max(0, min(32, t.row_end - rbase)) : 0;
+        uint8_t* base = reinterpret_cast<uint8_t*>(out + (size_t)rbase * ldo + t.n * kBNx + half * 128);
+        uint8_t* stg = s_stage_out + (warp - 3) * kStgWarp;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float* a = acc + 32 * c + 8 * j;
-            uint4 w;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(a[4], a[5]);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(a[6], a[7]);
-            w.x = *reinterpret_cast<uint32_t*>(&h0);
-            w.y = *reinterpret_cast<uint32_t*>(&h1);
-            w.z = *reinterpret_cast<uint32_t*>(&h2);
-            w.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = w;
-          }
-          __syncwarp();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = 8 * k + (lane >> 2), j = lane & 3;
-            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
-            if (ok && rbase + r < t.row_end)
-              *reinterpret_cast<uint4*>(out + (size_t)(rbase + r) * ldo + col0 + 32 * c + 8 * j) = w;
-          }
-          __syncwarp();
+          uint4 w[4];
+          pack_bf16x32(acc + 32 * c, w);
+          warp_store_rows64(stg, lane, w, base + c * 64, (size_t)ldo * 2, nrows);
         }
       }
     }

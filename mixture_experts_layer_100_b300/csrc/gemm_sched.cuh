@@ -78,6 +78,45 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
   }
 }
 
+// Bytes of shared memory one warp needs for warp_store_rows64.
+constexpr int kRowStageBytes = 2048;
+
+// Writes 64 bytes of each of a warp's 32 rows (lane r holds row r's bytes in
+// w[0..3]) to base + r * pitch, passing them through a 2 KB staging block of
+// shared memory so that each store instruction covers 8 rows x 64 contiguous
+// bytes instead of 32 rows x 16 bytes. Staging layout: row r, 16-byte chunk j
+// at r * 64 + (j ^ ((r >> 1) & 3)) * 16, conflict-free for both the row-wise
+// writes and the chunk-wise reads. Rows r >= nrows are not stored. Every lane
+// of the warp must call it.
+__device__ __forceinline__ void warp_store_rows64(uint8_t* stg, int lane, const uint4 (&w)[4], uint8_t* base,
+                                                  size_t pitch, int nrows) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = w[j];
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2), j = lane & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+    if (r < nrows) *reinterpret_cast<uint4*>(base + (size_t)r * pitch + 16 * j) = v;
+  }
+  __syncwarp();
+}
+
+// 32 fp32 values -> 32 bf16 (round to nearest even) packed in four 16-byte words.
+__device__ __forceinline__ void pack_bf16x32(const float* v, uint4 (&w)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+    w[q].x = *reinterpret_cast<uint32_t*>(&h0);
+    w[q].y = *reinterpret_cast<uint32_t*>(&h1);
+    w[q].z = *reinterpret_cast<uint32_t*>(&h2);
+    w[q].w = *reinterpret_cast<uint32_t*>(&h3);
+  }
+}
+
 __device__ __forceinline__ void add_bf16x32(float* acc, const __nv_bfloat16* src, float g) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll

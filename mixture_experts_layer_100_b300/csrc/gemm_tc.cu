@@ -23,7 +23,7 @@ struct Cfg {
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes + 4 * kRowStageBytes;
 };
 
 template <int BN, Epi EPI>
@@ -249,9 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
-      const int row = t.row0 + 32 * q + lane;
+      const int rbase = t.row0 + 32 * q;
+      const int row = rbase + lane;
       const bool valid = row < t.row_end;
-      tile_epilogue<BN, EPI>(p, t, tbase, row, valid);
+      const int nrows = max(0, min(32, t.row_end - rbase));
+      tile_epilogue<BN, EPI>(p, t, tbase, row, valid, aux + kAuxBytes + (warp - 2) * kRowStageBytes, rbase, nrows);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
