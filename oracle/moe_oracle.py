@@ -247,6 +247,39 @@ def load_max_over_mean(counts: np.ndarray, T: int, K: int) -> float:
     return float(F32(counts.max() * len(counts) / (T * K)))
 
 
+def sequence_balance(scores: np.ndarray, topk_idx: np.ndarray, seq_len: int, alpha: float):
+    """Sequence-wise balance statistic of the routing [digest-2.2]: the pages
+    keep a sequence-level balance loss with a very small weight but print no
+    formula; this is the DeepSeek-V3 report's definition (the report the
+    pages digest), read forward-only. For each run of seq_len consecutive
+    tokens (the last run may be shorter), with L its length, E experts and K
+    per token:
+        f_i = E / (K L) * #{t : expert i among the K chosen for token t}
+        P_i = (1 / L) * sum_t s_{i,t} / sum_j s_{j,t}
+        loss = alpha * sum_i f_i P_i
+    s are the raw sigmoid affinities, the chosen experts those of topk_idx.
+    Returns (loss [n_seq], f [n_seq, E], P [n_seq, E]) in float64.
+    """
+    s = np.asarray(scores, F64)
+    idx = np.asarray(topk_idx)
+    T, E = s.shape
+    K = idx.shape[1]
+    n_seq = (T + seq_len - 1) // seq_len
+    loss = np.zeros(n_seq)
+    f = np.zeros((n_seq, E))
+    P = np.zeros((n_seq, E))
+    for q in range(n_seq):
+        rows = slice(q * seq_len, min(T, (q + 1) * seq_len))
+        L = rows.stop - rows.start
+        chosen = np.zeros(E)
+        for e in idx[rows].ravel():
+            chosen[e] += 1
+        f[q] = E / (K * L) * chosen
+        P[q] = (s[rows] / s[rows].sum(axis=1, keepdims=True)).sum(axis=0) / L
+        loss[q] = alpha * float((f[q] * P[q]).sum())
+    return loss, f, P
+
+
 def bias_balancing_loop(scores: np.ndarray, bias0: np.ndarray, steps: int,
                         gamma: float, G: int, K: int, M: int, group_topk=2):
     """Repeated route -> count -> bias update on fixed scores.

@@ -241,3 +241,58 @@ def test_bias_checkpoint_round_trip():
         state.load_bias(b"XXXX" + blob[4:])
     with pytest.raises(ValueError):
         state.load_bias(blob[:-4])
+
+
+# --------------------------------------------------------------------------
+# sequence-wise balance statistic
+# --------------------------------------------------------------------------
+
+def test_sequence_balance_hand_example():
+    g = _golden("seq_balance_example.json")
+    loss, f, P = om.sequence_balance(np.array(g["scores"], F32), np.array(g["topk_idx"]), g["seq_len"], g["alpha"])
+    np.testing.assert_array_equal(f, np.array(g["f"], float))
+    np.testing.assert_allclose(P, [[n / d for n, d in row] for row in g["P_num_den"]], rtol=1e-15)
+    np.testing.assert_allclose(loss, [n / d for n, d in g["loss_num_den"]], rtol=1e-15)
+
+
+def test_sequence_balance_uniform_is_alpha():
+    """Equal affinities and perfectly even choices: f_i = 1, P_i = 1/E, so
+    the statistic is alpha exactly."""
+    T, E, K = 64, 16, 4
+    s = np.full((T, E), 0.3, F32)
+    idx = np.array([[(4 * t + k) % E for k in range(K)] for t in range(T)])  # every expert 16 times
+    loss, f, P = om.sequence_balance(s, idx, T, 0.01)
+    np.testing.assert_allclose(f, 1.0, rtol=1e-15)
+    np.testing.assert_allclose(P, 1.0 / E, rtol=1e-12)
+    np.testing.assert_allclose(loss, [0.01], rtol=1e-12)
+
+
+def test_sequence_balance_invariants_and_loops():
+    rng = np.random.default_rng(31)
+    T, E, K, L = 300, 32, 6, 128          # runs of 128, 128, 44
+    s = rng.uniform(0.01, 1.0, (T, E)).astype(F32)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+    loss, f, P = om.sequence_balance(s, idx, L, 1e-3)
+    assert loss.shape == (3,)
+    np.testing.assert_allclose(f.sum(axis=1), E, rtol=1e-12)    # sum_i f_i = E
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=1e-12)  # sum_i P_i = 1
+    # plain loops over the definition
+    for q, (a, b) in enumerate([(0, 128), (128, 256), (256, 300)]):
+        n = b - a
+        want = 0.0
+        for i in range(E):
+            c = sum(1 for t in range(a, b) for k in range(K) if idx[t, k] == i)
+            p = sum(float(s[t, i]) / sum(float(v) for v in s[t]) for t in range(a, b)) / n
+            want += (E / (K * n)) * c * p
+        assert abs(loss[q] - 1e-3 * want) <= 1e-12 * abs(want)
+
+
+def test_sequence_balance_concentrated():
+    """Every token chooses experts 0..K-1 and puts all its affinity mass
+    there: f_i = E/K and P_i = 1/K on those, so the statistic is alpha * E / K."""
+    T, E, K = 40, 16, 4
+    s = np.zeros((T, E), F32)
+    s[:, :K] = 0.25
+    idx = np.tile(np.arange(K), (T, 1))
+    loss, _, _ = om.sequence_balance(s, idx, T, 0.5)
+    np.testing.assert_allclose(loss, [0.5 * E / K], rtol=1e-12)
