@@ -194,6 +194,22 @@ moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int col
 moe_status moe_quantize_weights_e4m3_ue8m0(const void* w, int n_mat, int rows, int cols,
                                            uint8_t* q, float* scale, moe_stream_t stream);
 
+/* Sequence-wise balance statistic of a routing [digest-2.2: the sequence-level
+ * balance loss kept with a tiny weight; its formula is the DeepSeek-V3
+ * report's]. For each run of seq_len consecutive tokens (the last run may be
+ * shorter; L = its length):
+ *   f_i  = E / (K L) * (number of tokens of the run whose K choices include i)
+ *   P_i  = (1 / L) * sum_t s_{i,t} / sum_j s_{j,t}     (raw affinities)
+ *   loss = alpha * sum_i f_i P_i
+ *   scores:   [T, E] fp32 affinities, device, 16-byte aligned; NULL to use the
+ *             ones the last moe_route / moe_layer_forward call on ws left there
+ *   topk_idx: [T, K] int32 chosen experts (entries outside [0, E) are not counted)
+ *   loss:     [ceil(T/seq_len)] fp32 out; f, p: [ceil(T/seq_len), E] fp32 out
+ *             or NULL. Forward only (no gradient); deterministic.
+ * MOE_ERR_INVALID_ARG for seq_len <= 0 or bad pointers. */
+moe_status moe_seq_balance(const moe_config* cfg, const float* scores, const int32_t* topk_idx, int seq_len,
+                           float alpha, float* loss, float* f, float* p, void* ws, moe_stream_t stream);
+
 /* Bytes of the fixed device array that moe_permute_static uses as scratch. */
 #define MOE_PERMUTE_STATIC_SCRATCH_BYTES (4u << 20)
 

@@ -59,6 +59,7 @@ _SIGS = {
     "moe_quantize_weights_e4m3": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
     "moe_quantize_weights_e4m3_ue8m0": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
     "moe_permute_static": [ctypes.POINTER(moe_config)] + [_P] * 7 + [_P],
+    "moe_seq_balance": [ctypes.POINTER(moe_config), _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, _P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_selftest_timeout": [_P, _P],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
@@ -170,6 +171,15 @@ def moe_quantize_weights_e4m3_ue8m0(w, q, scale, stream=None):
     n_mat, rows, cols = w.shape
     _check("moe_quantize_weights_e4m3_ue8m0", lib.moe_quantize_weights_e4m3_ue8m0(
         _ptr(w), n_mat, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_seq_balance(cfg, scores, topk_idx, seq_len: int, alpha: float, loss, f=None, p=None, ws=None,
+                    stream=None):
+    """Per-run sequence-wise balance statistic; scores None reads the
+    affinities left in ws by the last routing call."""
+    _check("moe_seq_balance", lib.moe_seq_balance(
+        ctypes.byref(cfg), _ptr(scores), _ptr(topk_idx), int(seq_len), ctypes.c_float(alpha), _ptr(loss), _ptr(f),
+        _ptr(p), _ptr(ws), _stream(stream)))
 
 
 def moe_set_stage_events(events) -> None:

@@ -743,6 +743,24 @@ moe_status moe_quantize_weights_e4m3_ue8m0(const void* w, int n_mat, int rows, i
   return quantize_weights(w, n_mat, rows, cols, q, scale, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_seq_balance(const moe_config* cfg, const float* scores, const int32_t* topk_idx, int seq_len,
+                           float alpha, float* loss, float* f, float* p, void* ws, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config& c = *cfg;
+  if (seq_len <= 0) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (scores == nullptr) {
+    if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+    scores = at<float>(ws, layout(c).scores);
+  }
+  if (!aligned16(scores) || !ok_ptr(topk_idx) || loss == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(loss) | reinterpret_cast<uintptr_t>(f) | reinterpret_cast<uintptr_t>(p)) & 3u)
+    return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_seq_balance(scores, topk_idx, c.T, c.E, c.K, seq_len, alpha, loss, f, p,
+                              reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 moe_status moe_set_stage_events(void* const* events, int count) {
   if (count == 0) {
     g_stage_on = false;

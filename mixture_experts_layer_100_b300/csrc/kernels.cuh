@@ -13,6 +13,8 @@ namespace moe {
 cudaError_t launch_route_select(const float* scores, const float* bias, int T, int E, int G, int K, int M, int gk,
                                 int* topk_idx, float* topk_gate, int* counts, int num_sms, cudaStream_t st);
 cudaError_t launch_router_f32(const float* x, const float* wr, int T, int d, int E, float* scores, cudaStream_t st);
+cudaError_t launch_seq_balance(const float* scores, const int* topk_idx, int T, int E, int K, int seq_len,
+                               float alpha, float* loss, float* f, float* p, cudaStream_t st);
 
 // ---- permutation (permute.cu)
 int permute_chunks(int T);

@@ -195,7 +195,84 @@ __global__ void __launch_bounds__(256) router_f32_kernel(const float* __restrict
   }
 }
 
+// Sequence-wise balance statistic of the routing (the DeepSeek-V3 report's
+// sequence-level balance loss, which the digest's section 2.2 keeps with a
+// tiny weight), one block per run of seq_len tokens:
+//   f_i = E / (K L) * (times expert i is chosen), P_i = (1/L) sum_t s_it / sum_j s_jt,
+//   loss = alpha * sum_i f_i P_i.
+// Deterministic: row sums by a fixed warp butterfly, each (phase, expert)
+// thread sums its tokens in order, partials are combined in a fixed order.
+constexpr int kBalThreads = 1024;
+constexpr int kBalChunk = 1024;  // tokens whose row sums are staged at a time
+
+__global__ void __launch_bounds__(kBalThreads)
+    seq_balance_kernel(const float* __restrict__ scores, const int* __restrict__ topk_idx, int T, int E, int K,
+                       int seq_len, float alpha, float* __restrict__ loss, float* __restrict__ f_out,
+                       float* __restrict__ p_out) {
+  __shared__ float rs[kBalChunk];
+  __shared__ float part[kBalThreads];
+  __shared__ int cnt[512];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * seq_len;
+  const int L = min(seq_len, T - t0);
+  const int nph = kBalThreads / E;  // token phases per expert (E <= 512)
+  const int e = tid % E, ph = tid / E;
+  const bool active = ph < nph;
+  for (int i = tid; i < E; i += kBalThreads) cnt[i] = 0;
+  __syncthreads();
+  const int* idx = topk_idx + (size_t)t0 * K;
+  for (int i = tid; i < L * K; i += kBalThreads) {
+    const int x = idx[i];
+    if (x >= 0 && x < E) atomicAdd(&cnt[x], 1);
+  }
+  float acc = 0.0f;
+  for (int c0 = 0; c0 < L; c0 += kBalChunk) {
+    const int n = min(kBalChunk, L - c0);
+    for (int tt = warp; tt < n; tt += kBalThreads / 32) {
+      const float* row = scores + (size_t)(t0 + c0 + tt) * E;
+      float v = 0.0f;
+      for (int j = lane; j < E; j += 32) v += row[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) rs[tt] = v;
+    }
+    __syncthreads();
+    if (active)
+      for (int tt = ph; tt < n; tt += nph) acc += __fdiv_rn(scores[(size_t)(t0 + c0 + tt) * E + e], rs[tt]);
+    __syncthreads();
+  }
+  part[tid] = active ? acc : 0.0f;
+  __syncthreads();
+  float contrib = 0.0f;
+  if (tid < E) {
+    float P = 0.0f;
+    for (int q = 0; q < nph; ++q) P += part[q * E + tid];
+    P = __fdiv_rn(P, (float)L);
+    const float f = (float)((double)E * cnt[tid] / ((double)K * L));
+    if (f_out) f_out[(size_t)blockIdx.x * E + tid] = f;
+    if (p_out) p_out[(size_t)blockIdx.x * E + tid] = P;
+    contrib = f * P;
+  }
+  __syncthreads();
+  part[tid] = contrib;
+  __syncthreads();
+  for (int w = kBalThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) part[tid] += part[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0) loss[blockIdx.x] = alpha * part[0];
+}
+
 }  // namespace
+
+cudaError_t launch_seq_balance(const float* scores, const int* topk_idx, int T, int E, int K, int seq_len,
+                               float alpha, float* loss, float* f, float* p, cudaStream_t st) {
+  if (E > 512 || seq_len <= 0) return cudaErrorInvalidValue;
+  const int n_seq = (T + seq_len - 1) / seq_len;
+  if (n_seq == 0) return cudaSuccess;
+  seq_balance_kernel<<<n_seq, kBalThreads, 0, st>>>(scores, topk_idx, T, E, K, seq_len, alpha, loss, f, p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route_select(const float* scores, const float* bias, int T, int E, int G, int K, int M, int gk,
                                 int* topk_idx, float* topk_gate, int* counts, int num_sms, cudaStream_t st) {
