@@ -144,9 +144,9 @@ def dist_env():
 # depends on, per expert-GEMM dtype (profiles/traffic.json, key
 # "gemm1_swiglu:<dtype>")
 TRAFFIC_SOURCES = {
-    "bf16": ("gemm_tc.cu", "gemm_epi.cuh", "gemm_sched.cuh", "api.cu"),
-    "e4m3": ("gemm_fp8.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "api.cu"),
-    "e4m3_ue8m0": ("gemm_mx.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "api.cu"),
+    "bf16": ("gemm_tc.cu", "gemm_epi.cuh", "gemm_sched.cuh", "stages.cu"),
+    "e4m3": ("gemm_fp8.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "stages.cu"),
+    "e4m3_ue8m0": ("gemm_mx.cu", "gemm_fp8.cuh", "gemm_sched.cuh", "stages.cu"),
 }
 
 
