@@ -177,3 +177,61 @@ def test_v3_ue8m0_preset_sampled_tokens():
     assert res["counts"].sum().item() == p.T * p.K
     del w, wq
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [1, 129])
+def test_ue8m0_layer_one_token_and_ragged(T):
+    """One token (every tile mostly padding) and one row past a whole tile."""
+    p = small("t300_d256_e16_i256", T=T)
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    res = run_layer(p, quantize_device_weights(device_weights(w), ue8m0=True), x.to(DEV), b.to(DEV))
+    compare(p, res, oracle_rows_fp8(p, w, x, b), b, dtype="e4m3_ue8m0")
+
+
+def test_ue8m0_all_tokens_on_four_experts():
+    """Bias +1 on group 0: four experts take all T = 1000 rows each (eight
+    m-tiles per expert, the last one ragged); the others get none."""
+    p = small("t300_d256_e16_i256", T=1000)
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = torch.zeros(p.E)
+    b[:4] = 1.0
+    res = run_layer(p, quantize_device_weights(device_weights(w), ue8m0=True), x.to(DEV), b.to(DEV))
+    c = res["counts"].cpu().numpy()
+    assert list(c[:4]) == [p.T] * 4 and c[4:].sum() == 0
+    compare(p, res, oracle_rows_fp8(p, w, x, b), b, dtype="e4m3_ue8m0")
+
+
+def test_ue8m0_zero_routed_weights_give_shared_only():
+    """All-zero routed weights quantise to all-zero blocks with scale 1; the
+    output is the shared experts' FP8 output alone."""
+    p = small("t515_d512_e32_i384_s2")
+    w = synth.make_weights(p, zero_routed=True)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    wq = quantize_device_weights(device_weights(w), ue8m0=True)
+    assert torch.all(wq["w13_scale"] == 1.0) and torch.all(wq["w2_scale"] == 1.0)
+    res = run_layer(p, wq, x.to(DEV), b.to(DEV))
+    qx, sx = om.quantize_rows_1x128(x.float().numpy(), ue8m0=True)
+    shared = sum(om.swiglu_ffn_fp8(qx, sx, *om.quantize_expert_weights(w.ws13[i].float().numpy(),
+                                                                      w.ws2[i].float().numpy(), ue8m0=True),
+                                   ue8m0=True) for i in range(p.S))
+    got = res["out"].float().cpu().numpy()
+    assert np.abs(got - shared).max() / np.abs(shared).max() <= 6e-2
+
+
+def test_ue8m0_empty_batch_is_a_no_op():
+    from mixture_experts_layer_100_b300 import binding as B
+    p = small("t300_d256_e16_i256", T=0)
+    w = synth.make_weights(p.replace(T=1))
+    cfg = B.config_from_preset(p)
+    ws = B.alloc_workspace(cfg)
+    b = torch.zeros(p.E, device=DEV)
+    counts = torch.full((p.E,), 5, dtype=torch.int32, device=DEV)
+    dummy = torch.empty(16, dtype=torch.int32, device=DEV)
+    wq = quantize_device_weights(device_weights(w), ue8m0=True)
+    B.moe_layer_forward(cfg, None, B.make_weights(**wq), b, 1e-3, None, dummy, dummy.float(), counts, None, ws)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0 and b.abs().sum().item() == 0
