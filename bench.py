@@ -37,8 +37,6 @@ METRIC = "MoE-layer tokens/sec (1×B300, V3 shape T=16K bf16); % tensor/HBM roof
 DEFAULT_PRESET = "v3_t16384_d7168_e256_bf16"
 STAGES = ["router_gemm", "route_select", "permute", "gemm1_swiglu", "gemm2_routed", "gemm2_shared_combine",
           "bias_update"]
-KERNELS_PER_STEP = 11  # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, routed sum,
-#                        gemm2+combine, bias
 
 
 def parse():
@@ -54,6 +52,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-standalone", action="store_true",
+                    help="skip the standalone timing of moe_route / moe_permute")
     return ap.parse_args()
 
 
@@ -332,6 +332,72 @@ def run_e2e(a, p, x, out, step, dev, pg):
                     "batches overlap the layer (3 streams, double buffers)"}
 
 
+def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps=20):
+    """moe_route (router GEMM + selection) and moe_permute timed on their own
+    (CUDA events, main stream, nothing else running), with their algorithmic
+    HBM bytes: the memory-bound part of the step without the side-stream
+    overlap of the layer call. Inputs are the bench's; outputs go to buffers
+    of their own."""
+    dev = x.device
+    T, E, K, d = p.T, p.E, p.K, p.d
+    a_b = 2 if p.dtype == "bf16" else 4
+    ex = 1 if f8 else a_b
+    scores = torch.empty(T, E, device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, K, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    st = torch.empty(T * K, dtype=torch.int32, device=dev)
+    sp = torch.empty(T, K, dtype=torch.int32, device=dev)
+    xp = torch.empty(T * K, d, dtype=torch.uint8 if f8 else x.dtype, device=dev)
+    xs = torch.empty(d // 128, T * K, device=dev) if f8 else None
+    b = bias.clone()
+
+    def route():
+        B.moe_route(cfg, x, w_router, None, b, scores, idx, gate, counts, ws)
+
+    def permute():
+        B.moe_permute(cfg, idx, counts, off, st, sp, x, xp, xs, ws)
+
+    out = {}
+    route_bytes = T * d * a_b + E * d * a_b + 2 * T * E * 4 + T * K * 8
+    perm_bytes = T * d * a_b + T * K * d * ex + T * K * 16 + (T * K * (d // 128) * 4 if f8 else 0)
+    for name, fn, nbytes in (("route", route, route_bytes), ("permute", permute, perm_bytes)):
+        for _ in range(3):
+            route()
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    tot_b = route_bytes + perm_bytes
+    tot_ms = out["route"]["ms"] + out["permute"]["ms"]
+    out["route_permute"] = {"gbs": tot_b / (tot_ms * 1e-3) / 1e9, "frac_hbm": tot_b / (tot_ms * 1e-3) / 1e9 / hbm}
+    code = B.moe_device_error(ws)
+    if code != 0:
+        raise RuntimeError(f"device error 0x{code:x} in the standalone stages")
+    return out
+
+
+def kernels_per_step(p):
+    """Kernels of this library one moe_layer_forward step launches."""
+    if p.dtype == "f32":
+        # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, combine, bias update
+        return 10 - (1 if p.S == 0 else 0)
+    n = 11  # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, routed sum, combine, bias update
+    if p.S == 0:
+        n -= 2  # no shared gemm1; the routed sum writes the output
+    if p.expert_dtype in ("e4m3", "e4m3_ue8m0"):
+        n += 1 + (1 if p.S > 0 else 0)  # tile-major scale layout; x quantised for the shared experts
+    return n
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(a, p):
     from mixture_experts_layer_100_b300 import binding as B
@@ -454,6 +520,10 @@ def run_ours(a, p):
     mem_ms = stage_ms["router_gemm"] + stage_ms["route_select"] + stage_ms["permute"]
     mem_gbs = (hb["router_gemm"] + hb["route_select"] + hb["permute"]) / (mem_ms * 1e-3) / 1e9
 
+    standalone = None
+    if rank == 0 and not a.no_standalone:
+        standalone = run_standalone_memory_stages(B, cfg, p, x, wd["w_router"], bias, ws, f8, hbm)
+
     e2e = None
     if not a.no_e2e:
         e2e = run_e2e(a, p, x, out, step, dev, pg)
@@ -483,10 +553,13 @@ def run_ours(a, p):
             "stages": stages,
             "expert_gemms": {"tflops": expert_gemm_tf, "frac_tensor_sustained": expert_gemm_tf / tf_sust,
                              "frac_tensor_burst": expert_gemm_tf / tf_burst},
-            "route_permute_hbm": {"gbs": mem_gbs, "frac_hbm": mem_gbs / hbm},
+            "route_permute_hbm": {"gbs": mem_gbs, "frac_hbm": mem_gbs / hbm,
+                                  "note": "stage times inside the step, where the shared experts' GEMM1 runs "
+                                          "beside routing and permutation on a side stream"},
+            "memory_stages_standalone": standalone,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP * K,
+            "gpu_launches": kernels_per_step(p) * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
