@@ -333,11 +333,11 @@ def run_e2e(a, p, x, out, step, dev, pg):
 
 
 def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps=20):
-    """moe_route (router GEMM + selection) and moe_permute timed on their own
-    (CUDA events, main stream, nothing else running), with their algorithmic
-    HBM bytes: the memory-bound part of the step without the side-stream
-    overlap of the layer call. Inputs are the bench's; outputs go to buffers
-    of their own."""
+    """moe_route (router GEMM + selection), moe_permute and the routed sum of
+    moe_combine timed on their own (CUDA events, main stream, nothing else
+    running), with their algorithmic HBM bytes: the memory-bound part of the
+    step without the side-stream overlap of the layer call. Inputs are the
+    bench's; outputs go to buffers of their own."""
     dev = x.device
     T, E, K, d = p.T, p.E, p.K, p.d
     a_b = 2 if p.dtype == "bf16" else 4
@@ -359,12 +359,25 @@ def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps
     def permute():
         B.moe_permute(cfg, idx, counts, off, st, sp, x, xp, xs, ws)
 
+    # the memory-bound part of the combine: the gate-weighted sum of each
+    # token's K expert rows, which moe_combine runs alone for S = 0
+    cfg0 = B.make_config(T, d, E, p.G, K, p.M, p.I, 0, p.group_topk, p.dtype, p.expert_dtype)
+    yp = torch.zeros(T * K, d, dtype=x.dtype, device=dev)
+    rsum = torch.empty(T, d, dtype=x.dtype, device=dev)
+    no_w = B.make_weights()
+
+    def combine():
+        B.moe_combine(cfg0, yp, sp, gate, None, no_w, rsum, ws)
+
     out = {}
     route_bytes = T * d * a_b + E * d * a_b + 2 * T * E * 4 + T * K * 8
     perm_bytes = T * d * a_b + T * K * d * ex + T * K * 16 + (T * K * (d // 128) * 4 if f8 else 0)
-    for name, fn, nbytes in (("route", route, route_bytes), ("permute", permute, perm_bytes)):
+    comb_bytes = T * K * d * a_b + T * d * a_b + T * K * 8
+    for name, fn, nbytes in (("route", route, route_bytes), ("permute", permute, perm_bytes),
+                             ("combine_routed_sum", combine, comb_bytes)):
         for _ in range(3):
             route()
+            permute()
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -379,6 +392,10 @@ def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps
     tot_b = route_bytes + perm_bytes
     tot_ms = out["route"]["ms"] + out["permute"]["ms"]
     out["route_permute"] = {"gbs": tot_b / (tot_ms * 1e-3) / 1e9, "frac_hbm": tot_b / (tot_ms * 1e-3) / 1e9 / hbm}
+    tot_b += comb_bytes
+    tot_ms += out["combine_routed_sum"]["ms"]
+    out["route_permute_combine"] = {"gbs": tot_b / (tot_ms * 1e-3) / 1e9,
+                                    "frac_hbm": tot_b / (tot_ms * 1e-3) / 1e9 / hbm}
     code = B.moe_device_error(ws)
     if code != 0:
         raise RuntimeError(f"device error 0x{code:x} in the standalone stages")
