@@ -399,9 +399,13 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       ptx::tc_fence_after();
       float acc[128];
       if (ok) {
+        // four loads in flight at once, then one wait: the accumulator goes
+        // back to the MMA warp after a single TMEM round trip
         const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + half * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tb + c * 32, acc + 32 * c);
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32_nowait(tb + c * 32, acc + 32 * c);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(acc + 32 * c);
       } else {
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
