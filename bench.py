@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-standalone", action="store_true",
                     help="skip the standalone timing of moe_route / moe_permute")
     return ap.parse_args()
@@ -402,6 +403,30 @@ def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps
     return out
 
 
+def run_graph_replay(step, p, K, dev, world):
+    """One layer step captured into a CUDA graph (after the eager steps above
+    created the library's side stream) and replayed K times, timed with CUDA
+    events: the same kernels without per-launch host work."""
+    if world != 1:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    return {"ms_per_step": ms, "value": p.T / (ms / 1000.0), "unit": "tokens/s", "steps": K,
+            "note": "moe_layer_forward captured once into a CUDA graph and replayed"}
+
+
 def kernels_per_step(p):
     """Kernels of this library one moe_layer_forward step launches."""
     if p.dtype == "f32":
@@ -537,6 +562,13 @@ def run_ours(a, p):
     mem_ms = stage_ms["router_gemm"] + stage_ms["route_select"] + stage_ms["permute"]
     mem_gbs = (hb["router_gemm"] + hb["route_select"] + hb["permute"]) / (mem_ms * 1e-3) / 1e9
 
+    graph = None
+    if not a.no_graph:
+        graph = run_graph_replay(step, p, K, dev, world)
+        code = B.moe_device_error(ws)
+        if code != 0:
+            raise RuntimeError(f"device error 0x{code:x} in the graph replay")
+
     standalone = None
     if rank == 0 and not a.no_standalone:
         standalone = run_standalone_memory_stages(B, cfg, p, x, wd["w_router"], bias, ws, f8, hbm)
@@ -574,6 +606,7 @@ def run_ours(a, p):
                                   "note": "stage times inside the step, where the shared experts' GEMM1 runs "
                                           "beside routing and permutation on a side stream"},
             "memory_stages_standalone": standalone,
+            "graph_replay": graph,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": kernels_per_step(p) * K,

@@ -60,6 +60,21 @@ __device__ __forceinline__ float e4m3_tile_scale(float amax, bool ue8m0) {
 // The mantissa bits of any other value are ignored.
 __device__ __forceinline__ uint32_t ue8m0_byte(float s) { return (__float_as_uint(s) >> 23) & 0xFFu; }
 
+// Raises the dynamic shared-memory limit of `kern` on the current device the
+// first time it is asked there (`done` is one array per kernel
+// instantiation), so that later launches, including launches issued while a
+// stream is being captured into a CUDA graph, make no attribute call.
+template <typename F>
+inline cudaError_t set_smem_once(F kern, int bytes, int (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
 // e4m3 code of v (round to nearest even, saturating to +/-448).
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
   return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);

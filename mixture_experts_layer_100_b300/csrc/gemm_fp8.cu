@@ -370,7 +370,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
 template <Fp8Epi EPI>
 cudaError_t launch_fp8_one(const Fp8GemmLaunch& L) {
   auto kern = tc_gemm_fp8_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem8);
+  static int attr_done[64] = {};
+  cudaError_t e = set_smem_once(kern, kSmem8, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kThreads8, kSmem8, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
   return cudaGetLastError();

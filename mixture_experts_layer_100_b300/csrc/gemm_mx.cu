@@ -492,7 +492,8 @@ __global__ void __launch_bounds__(kThreadsX, 1)
 template <Fp8Epi EPI>
 cudaError_t launch_mx_one(const Fp8GemmLaunch& L) {
   auto kern = tc_gemm_mx_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemX);
+  static int attr_done[64] = {};
+  cudaError_t e = set_smem_once(kern, kSmemX, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kThreadsX, kSmemX, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
   return cudaGetLastError();

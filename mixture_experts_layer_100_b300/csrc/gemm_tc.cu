@@ -273,7 +273,8 @@ template <int BN, Epi EPI>
 cudaError_t launch_one(const TcGemmLaunch& L) {
   auto kern = tc_gemm_kernel<BN, EPI>;
   constexpr int smem = Cfg<BN>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static int attr_done[64] = {};
+  cudaError_t e = set_smem_once(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kThreads, smem, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
   return cudaGetLastError();
