@@ -11,9 +11,14 @@
 // fp32 registers, so the scaled sum over K blocks is formed outside the
 // tensor core at full fp32 precision while the next block is multiplied.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
-// epilogue; warp w drains TMEM lane quarter w % 4, column half (w - 2) / 4
-// (128 of the tile's 256 columns), and keeps 128 fp32 accumulators.
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps;
+// epilogue warp w drains TMEM lane quarter w % 4. GEMM1 (SwiGLU, 320
+// threads): 8 epilogue warps, column half (w - 2) / 4 (128 of the tile's 256
+// columns), 128 fp32 accumulators each. Down projections (576 threads): 16
+// epilogue warps, column slice (w - 2) / 4 (64 columns), 64 accumulators
+// each, loaded 16 columns at a time to fit 96 registers: the drain of a K
+// block is spread over twice the warps, which pays for their short K (a
+// quarter of GEMM1's blocks per tile); on GEMM1 it measured slower.
 #include "gemm_fp8.cuh"
 #include "gemm_sched.cuh"
 #include "ptx.cuh"
@@ -24,7 +29,11 @@ namespace {
 constexpr int kBK8 = 128;        // e4m3 elements per 128-byte swizzle row = one scale block
 constexpr int kUK8 = 32;         // K per tcgen05.mma kind::f8f6f4
 constexpr int kBN8 = 256;
-constexpr int kThreads8 = 320;
+template <Fp8Epi EPI>
+struct F8Cfg {
+  static constexpr int kEpiWarps = EPI == Fp8Epi::kSwiGLU ? 8 : 16;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+};
 constexpr int kABytes8 = kBM * 128;
 constexpr int kBBytes8 = kBN8 * 128;
 constexpr int kStage8 = kABytes8 + kBBytes8;
@@ -33,7 +42,7 @@ constexpr int kAux8 = 12288;
 constexpr int kSmem8 = 1024 + kStages8 * kStage8 + kAux8;
 
 __device__ __forceinline__ void epi_bar() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 epilogue warps
+  asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 epilogue warps (SwiGLU)
 }
 
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
@@ -42,7 +51,7 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 }
 
 template <Fp8Epi EPI>
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(F8Cfg<EPI>::kThreads, 1)
     tc_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                        const Fp8GemmParams p) {
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 8);
+      ptx::mbar_init(&tempty[a], F8Cfg<EPI>::kEpiWarps);
     }
     ptx::mbar_init(mma_done, 1);
     ptx::fence_barrier_init();
@@ -231,127 +240,264 @@ __global__ void __launch_bounds__(kThreads8, 1)
       if (!ptx::mbar_wait(mma_done, 0, nullptr)) set_error(p.err, kDevTimeoutDrain);
     }
   } else {
-    // ================= epilogue (warps 2..9)
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int r_in_tile = 32 * q + lane;
-    uint32_t g = 0;
-    bool ok = true;
-    for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
-      const Tile t = sch.decode(L);
-      const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
-      const int row = t.row0 + r_in_tile;
-      const int rows_total = t.seg ? p.rows1 : p.rows_total0;
-      const bool valid = row < t.row_end;
-      const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
-      // per-tile weight-scale addressing
-      const float* sb_base;
-      int sb_stride_kb = 1;
-      int rb0 = 0, rb1 = 0;  // scale rows (128-row weight blocks) for this half's two 64-col parts
-      if constexpr (EPI == Fp8Epi::kSwiGLU) {
-        const int nblk = p.I / 128;  // 128-row blocks per projection
-        int e, nn;
-        if (t.seg == 0) {
-          e = t.group;
-          nn = t.n;
-        } else {
-          e = t.n / nblk;
-          nn = t.n % nblk;
-        }
-        const int kbk = t.seg ? p.k_blocks1 : p.k_blocks0;  // d / 128
-        sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbk;
-        rb0 = nn;          // gate block
-        rb1 = nblk + nn;   // up block
-        sb_stride_kb = kbk;
-      } else {
-        const int nbd = p.N / 128;  // d / 128 row blocks of W2
-        const int kpe = p.I / 128;  // K blocks per expert
-        sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
-        rb0 = rb1 = t.n * 2 + half;
-        sb_stride_kb = kpe;
-      }
-      float acc[128];
-#pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-      for (int kb = 0; kb < kbs; ++kb, ++g) {
-        const uint32_t b = g & 1;
-        if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
-          set_error(p.err, kDevTimeoutEpilogue);
-          ok = false;
-        }
-        ptx::tc_fence_after();
-        const float sa = (row < rows_total && ok) ? __ldg(sa_base + (size_t)kb * rows_total + row) : 0.0f;
-        float f0, f1;
+    if constexpr (EPI == Fp8Epi::kSwiGLU) {
+      // ================= epilogue (warps 2..9)
+      const int q = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int r_in_tile = 32 * q + lane;
+      uint32_t g = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
+        const Tile t = sch.decode(L);
+        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
+        const int row = t.row0 + r_in_tile;
+        const int rows_total = t.seg ? p.rows1 : p.rows_total0;
+        const bool valid = row < t.row_end;
+        const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
+        // per-tile weight-scale addressing
+        const float* sb_base;
+        int sb_stride_kb = 1;
+        int rb0 = 0, rb1 = 0;  // scale rows (128-row weight blocks) for this half's two 64-col parts
         if constexpr (EPI == Fp8Epi::kSwiGLU) {
-          f0 = sa * __ldg(sb_base + (size_t)rb0 * sb_stride_kb + kb);
-          f1 = sa * __ldg(sb_base + (size_t)rb1 * sb_stride_kb + kb);
+          const int nblk = p.I / 128;  // 128-row blocks per projection
+          int e, nn;
+          if (t.seg == 0) {
+            e = t.group;
+            nn = t.n;
+          } else {
+            e = t.n / nblk;
+            nn = t.n % nblk;
+          }
+          const int kbk = t.seg ? p.k_blocks1 : p.k_blocks0;  // d / 128
+          sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbk;
+          rb0 = nn;          // gate block
+          rb1 = nblk + nn;   // up block
+          sb_stride_kb = kbk;
         } else {
-          // shared segment: K runs over S experts of I columns each
-          const int e = t.seg ? (kb * 128) / p.I : 0;
-          const int kk = t.seg ? ((kb * 128) % p.I) / 128 : kb;
-          const float* sb = t.seg ? p.b_scale1 + (size_t)e * (p.N / 128) * (p.I / 128) : sb_base;
-          f0 = f1 = sa * __ldg(sb + (size_t)rb0 * sb_stride_kb + kk);
+          const int nbd = p.N / 128;  // d / 128 row blocks of W2
+          const int kpe = p.I / 128;  // K blocks per expert
+          sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
+          rb0 = rb1 = t.n * 2 + half;
+          sb_stride_kb = kpe;
         }
-        if (ok) {
-          const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8 + half * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            ptx::tmem_ld32(tb + c * 32, v);
-            const float f = (c < 2) ? f0 : f1;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(v[j], f, acc[c * 32 + j]);
+        float acc[128];
+  #pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        for (int kb = 0; kb < kbs; ++kb, ++g) {
+          const uint32_t b = g & 1;
+          if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
+            set_error(p.err, kDevTimeoutEpilogue);
+            ok = false;
+          }
+          ptx::tc_fence_after();
+          const float sa = (row < rows_total && ok) ? __ldg(sa_base + (size_t)kb * rows_total + row) : 0.0f;
+          float f0, f1;
+          if constexpr (EPI == Fp8Epi::kSwiGLU) {
+            f0 = sa * __ldg(sb_base + (size_t)rb0 * sb_stride_kb + kb);
+            f1 = sa * __ldg(sb_base + (size_t)rb1 * sb_stride_kb + kb);
+          } else {
+            // shared segment: K runs over S experts of I columns each
+            const int e = t.seg ? (kb * 128) / p.I : 0;
+            const int kk = t.seg ? ((kb * 128) % p.I) / 128 : kb;
+            const float* sb = t.seg ? p.b_scale1 + (size_t)e * (p.N / 128) * (p.I / 128) : sb_base;
+            f0 = f1 = sa * __ldg(sb + (size_t)rb0 * sb_stride_kb + kk);
+          }
+          if (ok) {
+            const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8 + half * 128;
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float v[32];
+              ptx::tmem_ld32(tb + c * 32, v);
+              const float f = (c < 2) ? f0 : f1;
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(v[j], f, acc[c * 32 + j]);
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+        }
+        if constexpr (EPI == Fp8Epi::kSwiGLU) {
+          // h = silu(gate) * up for this half's 64 intermediate columns, then the
+          // 1x128 e4m3 tile shared with the other half of the row
+          float amax = 0.0f;
+  #pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            acc[j] = silu(acc[j]) * acc[64 + j];
+            amax = fmaxf(amax, fabsf(acc[j]));
+          }
+          s_amax[half * 128 + r_in_tile] = amax;
+          epi_bar();
+          amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + r_in_tile]);
+          epi_bar();  // s_amax is rewritten by the next tile
+          const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+          if (valid) {
+            uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
+            const int ldo = t.seg ? p.ldo1 : p.ldo0;
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + half * 64);
+  #pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
+                               __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
+              w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
+                               __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
+              w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
+                               __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
+              w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
+                               __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
+              dst[v] = w;
+            }
+            if (half == 0) {
+              float* hs = t.seg ? p.out_scale1 : p.out_scale0;
+              hs[(size_t)t.n * rows_total + row] = scale;
+            }
+          }
+        } else {
+          if (valid) {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
+            const int ldo = t.seg ? p.ldo1 : p.ldo0;
+            const size_t o = (size_t)row * ldo + t.n * kBN8 + half * 128;
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
+              store_bf16x32(out + o + 32 * c, acc + 32 * c);
+            }
           }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&tempty[b]);
       }
-      if constexpr (EPI == Fp8Epi::kSwiGLU) {
-        // h = silu(gate) * up for this half's 64 intermediate columns, then the
-        // 1x128 e4m3 tile shared with the other half of the row
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          acc[j] = silu(acc[j]) * acc[64 + j];
-          amax = fmaxf(amax, fabsf(acc[j]));
-        }
-        s_amax[half * 128 + r_in_tile] = amax;
-        epi_bar();
-        amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + r_in_tile]);
-        epi_bar();  // s_amax is rewritten by the next tile
-        const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        if (valid) {
-          uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
-          const int ldo = t.seg ? p.ldo1 : p.ldo0;
-          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + half * 64);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
-                             __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
-            w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
-                             __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
-            w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
-                             __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
-            w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
-                             __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
-            dst[v] = w;
+    } else {
+      // ================= epilogue (warps 2..17)
+      const int q = warp & 3;
+      const int slice = (warp - 2) >> 2;  // 0..3
+      const int r_in_tile = 32 * q + lane;
+      // SwiGLU: this warp's 32 h columns are 32 slice .. 32 slice + 31 of the
+      // tile's 128; their gate accumulators start at column ga (B tile rows are
+      // [gate 0..63 | up 0..63 | gate 64..127 | up 64..127]), the up ones at ga + 64
+      const int ga = slice < 2 ? 32 * slice : 128 + 32 * (slice - 2);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
+        const Tile t = sch.decode(L);
+        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
+        const int row = t.row0 + r_in_tile;
+        const int rows_total = t.seg ? p.rows1 : p.rows_total0;
+        const bool valid = row < t.row_end;
+        const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
+        // per-tile weight-scale addressing
+        const float* sb_base;
+        int sb_stride_kb = 1;
+        int rb0 = 0, rb1 = 0;  // scale rows (128-row weight blocks) of this warp's two 32-column parts
+        if constexpr (EPI == Fp8Epi::kSwiGLU) {
+          const int nblk = p.I / 128;  // 128-row blocks per projection
+          int e, nn;
+          if (t.seg == 0) {
+            e = t.group;
+            nn = t.n;
+          } else {
+            e = t.n / nblk;
+            nn = t.n % nblk;
           }
-          if (half == 0) {
-            float* hs = t.seg ? p.out_scale1 : p.out_scale0;
-            hs[(size_t)t.n * rows_total + row] = scale;
-          }
+          const int kbk = t.seg ? p.k_blocks1 : p.k_blocks0;  // d / 128
+          sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbk;
+          rb0 = nn;          // gate block
+          rb1 = nblk + nn;   // up block
+          sb_stride_kb = kbk;
+        } else {
+          const int nbd = p.N / 128;  // d / 128 row blocks of W2
+          const int kpe = p.I / 128;  // K blocks per expert
+          sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
+          rb0 = rb1 = t.n * 2 + (slice >> 1);  // columns 64 slice .. 64 slice + 63
+          sb_stride_kb = kpe;
         }
-      } else {
-        if (valid) {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
-          const int ldo = t.seg ? p.ldo1 : p.ldo0;
-          const size_t o = (size_t)row * ldo + t.n * kBN8 + half * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
-            store_bf16x32(out + o + 32 * c, acc + 32 * c);
+        float acc[64];
+  #pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        for (int kb = 0; kb < kbs; ++kb, ++g) {
+          const uint32_t b = g & 1;
+          if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
+            set_error(p.err, kDevTimeoutEpilogue);
+            ok = false;
+          }
+          ptx::tc_fence_after();
+          const float sa = (row < rows_total && ok) ? __ldg(sa_base + (size_t)kb * rows_total + row) : 0.0f;
+          float f0, f1;
+          if constexpr (EPI == Fp8Epi::kSwiGLU) {
+            f0 = sa * __ldg(sb_base + (size_t)rb0 * sb_stride_kb + kb);
+            f1 = sa * __ldg(sb_base + (size_t)rb1 * sb_stride_kb + kb);
+          } else {
+            // shared segment: K runs over S experts of I columns each
+            const int e = t.seg ? (kb * 128) / p.I : 0;
+            const int kk = t.seg ? ((kb * 128) % p.I) / 128 : kb;
+            const float* sb = t.seg ? p.b_scale1 + (size_t)e * (p.N / 128) * (p.I / 128) : sb_base;
+            f0 = f1 = sa * __ldg(sb + (size_t)rb0 * sb_stride_kb + kk);
+          }
+          if (ok) {
+            const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8;
+            const uint32_t c0 = EPI == Fp8Epi::kSwiGLU ? ga : 64 * slice;
+            const uint32_t c1 = EPI == Fp8Epi::kSwiGLU ? ga + 64 : 64 * slice + 32;
+            // 16 columns per load keeps the temporaries within the 96
+            // registers a thread of a 576-thread block has
+  #pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              float v[16];
+              ptx::tmem_ld16(tb + (h < 2 ? c0 : c1) + 16 * (h & 1), v);
+              const float f = h < 2 ? f0 : f1;
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(v[j], f, acc[16 * h + j]);
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+        }
+        if constexpr (EPI == Fp8Epi::kSwiGLU) {
+          // h = silu(gate) * up for this warp's 32 intermediate columns, then
+          // the 1x128 e4m3 tile shared with the three other slices of the row
+          float amax = 0.0f;
+  #pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            acc[j] = silu(acc[j]) * acc[32 + j];
+            amax = fmaxf(amax, fabsf(acc[j]));
+          }
+          s_amax[slice * 128 + r_in_tile] = amax;
+          epi_bar();
+  #pragma unroll
+          for (int o = 0; o < 4; ++o) amax = fmaxf(amax, s_amax[o * 128 + r_in_tile]);
+          epi_bar();  // s_amax is rewritten by the next tile
+          const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+          if (valid) {
+            uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
+            const int ldo = t.seg ? p.ldo1 : p.ldo0;
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + slice * 32);
+  #pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint4 w;
+              w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
+                               __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
+              w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
+                               __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
+              w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
+                               __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
+              w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
+                               __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
+              dst[v] = w;
+            }
+            if (slice == 0) {
+              float* hs = t.seg ? p.out_scale1 : p.out_scale0;
+              hs[(size_t)t.n * rows_total + row] = scale;
+            }
+          }
+        } else {
+          if (valid) {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
+            const int ldo = t.seg ? p.ldo1 : p.ldo0;
+            const size_t o = (size_t)row * ldo + t.n * kBN8 + slice * 64;
+  #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
+              store_bf16x32(out + o + 32 * c, acc + 32 * c);
+            }
           }
         }
       }
@@ -373,7 +519,7 @@ cudaError_t launch_fp8_one(const Fp8GemmLaunch& L) {
   static int attr_done[64] = {};
   cudaError_t e = set_smem_once(kern, kSmem8, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kThreads8, kSmem8, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
+  kern<<<L.grid, F8Cfg<EPI>::kThreads, kSmem8, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
   return cudaGetLastError();
 }
 
