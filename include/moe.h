@@ -171,7 +171,10 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float g
  * host thread and device, created by the first call and kept until the
  * process exits) while `stream` routes and permutes; `stream` waits for it
  * before the combine, so the layer is complete when `stream` is. Make the
- * first call on a device outside stream capture.
+ * first call on a device outside stream capture; later calls may be
+ * captured into a CUDA graph (the side stream's fork and join become graph
+ * edges, and the call makes no allocation or attribute change) and the graph
+ * replayed, each replay one step on the buffers given at capture time.
  * out [T, d] in cfg->act; topk_idx, topk_gate, counts as in moe_route;
  * bias [E] fp32 is updated in place after routing when gamma != 0;
  * max_over_mean as in moe_bias_update (nullable). */
