@@ -27,6 +27,8 @@ SMALL = {
     "t129_d512_e64_s0": dict(T=129, d=512, E=64, G=8, K=6, M=3, I=256, S=0),
     "t200_d256_e128_k6": dict(T=200, d=256, E=128, G=8, K=6, M=3, I=128, S=1),
     "t333_d256_e32_nodesum": dict(T=333, d=256, E=32, G=4, K=4, M=2, I=128, S=1, group_topk=8),
+    "t150_d256_e64_k16": dict(T=150, d=256, E=64, G=4, K=16, M=2, I=128, S=1),
+    "t90_d256_e64_k32": dict(T=90, d=256, E=64, G=2, K=32, M=1, I=128, S=1),
 }
 
 

@@ -44,6 +44,8 @@ ROUTE_SHAPES = [
     (512, 32, 8, 4, 1),   # the largest supported expert count
     (64, 4, 6, 2, 16),    # group score = plain sum over the group (the pages' node score)
     (256, 8, 8, 4, 32),   # V3 shape with the plain node sum
+    (64, 4, 16, 2, 2),    # K = 16
+    (128, 4, 32, 4, 2),   # K = 32, the largest the library takes
 ]
 
 
