@@ -36,8 +36,6 @@ __device__ __forceinline__ int read_error(const int* err) {
   return err ? *reinterpret_cast<const volatile int*>(err) : 0;
 }
 
-__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
-
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Scale of one e4m3 tile whose largest magnitude is amax; 1 for an all-zero
