@@ -562,6 +562,20 @@ def run_ours(a, p):
     mem_ms = stage_ms["router_gemm"] + stage_ms["route_select"] + stage_ms["permute"]
     mem_gbs = (hb["router_gemm"] + hb["route_select"] + hb["permute"]) / (mem_ms * 1e-3) / 1e9
 
+    # sequence-wise balance statistic of the last step's routing (runs of
+    # 4096 tokens; alpha 1, so the value is sum_i f_i P_i itself)
+    seq_len = min(4096, p.T)
+    n_seq = (p.T + seq_len - 1) // seq_len
+    sb_loss = torch.empty(n_seq, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    B.moe_seq_balance(cfg, None, idx, seq_len, 1.0, sb_loss, None, None, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    seq_balance = {"seq_len": seq_len, "alpha": 1.0, "per_sequence": [round(v, 6) for v in sb_loss.tolist()],
+                   "ms": e0.elapsed_time(e1),
+                   "note": "moe_seq_balance on the last step's affinities and choices; 1.0 = perfectly even"}
+
     graph = None
     if not a.no_graph:
         graph = run_graph_replay(step, p, K, dev, world)
@@ -607,6 +621,7 @@ def run_ours(a, p):
                                           "beside routing and permutation on a side stream"},
             "memory_stages_standalone": standalone,
             "graph_replay": graph,
+            "seq_balance": seq_balance,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": kernels_per_step(p) * K,
