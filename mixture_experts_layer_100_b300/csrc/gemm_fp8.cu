@@ -11,14 +11,15 @@
 // fp32 registers, so the scaled sum over K blocks is formed outside the
 // tensor core at full fp32 precision while the next block is multiplied.
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps;
-// epilogue warp w drains TMEM lane quarter w % 4. GEMM1 (SwiGLU, 320
-// threads): 8 epilogue warps, column half (w - 2) / 4 (128 of the tile's 256
-// columns), 128 fp32 accumulators each. Down projections (576 threads): 16
-// epilogue warps, column slice (w - 2) / 4 (64 columns), 64 accumulators
-// each, loaded 16 columns at a time to fit 96 registers: the drain of a K
-// block is spread over twice the warps, which pays for their short K (a
-// quarter of GEMM1's blocks per tile); on GEMM1 it measured slower.
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2 and
+// 3 idle, warps 4..11 epilogue; epilogue warp w drains TMEM lane quarter
+// w % 4 and column half (w - 4) / 4 (128 of the tile's 256 columns) into 128
+// fp32 accumulators. setmaxnreg gives the epilogue warpgroups 232 registers a
+// thread (the control warpgroup keeps 40), so two 32-column TMEM loads stay
+// in flight without spilling; each K block's scales are loaded while the
+// block before it drains, and the accumulator buffer is released before the
+// last FMAs of the block. GEMM1 quantises h to e4m3 in its epilogue; the
+// down projections write bf16 rows through a staging block per warp.
 #include "gemm_fp8.cuh"
 #include "gemm_sched.cuh"
 #include "ptx.cuh"
@@ -29,17 +30,28 @@ namespace {
 constexpr int kBK8 = 128;        // e4m3 elements per 128-byte swizzle row = one scale block
 constexpr int kUK8 = 32;         // K per tcgen05.mma kind::f8f6f4
 constexpr int kBN8 = 256;
-template <Fp8Epi EPI>
+// Three warpgroups; setmaxnreg moves registers from the control warpgroup
+// (producer, MMA issuer, two idle warps) to the two epilogue warpgroups, so
+// that 128 accumulators and two 32-column TMEM loads in flight fit without
+// spilling.
 struct F8Cfg {
-  static constexpr int kEpiWarps = EPI == Fp8Epi::kSwiGLU ? 8 : 16;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kCtlWarps = 4;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 32 * (kCtlWarps + kEpiWarps);
+  static constexpr int kLaunchRegs = 168;  // 3 warps per SM sub-partition: 3 x 32 x 168 <= 16384
+  static constexpr int kCtlRegs = 40;
+  static constexpr int kEpiRegs = 232;
 };
+static_assert(F8Cfg::kThreads * F8Cfg::kLaunchRegs ==
+                  32 * F8Cfg::kCtlWarps * F8Cfg::kCtlRegs + 32 * F8Cfg::kEpiWarps * F8Cfg::kEpiRegs,
+              "the register split must hand out exactly the registers the block is launched with");
 constexpr int kABytes8 = kBM * 128;
 constexpr int kBBytes8 = kBN8 * 128;
 constexpr int kStage8 = kABytes8 + kBBytes8;
 constexpr int kStages8 = 4;
 constexpr int kAux8 = 12288;
-constexpr int kSmem8 = 1024 + kStages8 * kStage8 + kAux8;
+constexpr int kStg8 = F8Cfg::kEpiWarps * kRowStageBytes;  // bf16 output staging, one block per epilogue warp
+constexpr int kSmem8 = 1024 + kStages8 * kStage8 + kAux8 + kStg8;
 
 __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 epilogue warps (SwiGLU)
@@ -51,7 +63,7 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 }
 
 template <Fp8Epi EPI>
-__global__ void __launch_bounds__(F8Cfg<EPI>::kThreads, 1)
+__global__ void __launch_bounds__(F8Cfg::kThreads, 1)
     tc_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                        const Fp8GemmParams p) {
@@ -70,6 +82,7 @@ __global__ void __launch_bounds__(F8Cfg<EPI>::kThreads, 1)
   int* s_mt = s_tp + (kMaxGroups + 1);
   int* s_off = s_mt + kMaxGroups;
   float* s_amax = reinterpret_cast<float*>(s_off + kMaxGroups + 1);  // [2][128]
+  uint8_t* s_stage = aux + kAux8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(F8Cfg<EPI>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], F8Cfg<EPI>::kEpiWarps);
+      ptx::mbar_init(&tempty[a], F8Cfg::kEpiWarps);
     }
     ptx::mbar_init(mma_done, 1);
     ptx::fence_barrier_init();
@@ -146,359 +159,253 @@ __global__ void __launch_bounds__(F8Cfg<EPI>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ================= TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_parity = 0;
-      bool ok = true;
-      for (int L = blockIdx.x; L < sch.total && ok; L += gridDim.x) {
-        const Tile t = sch.decode(L);
-        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
-        const CUtensorMap* ma = t.seg ? &tmA1 : &tmA0;
-        const CUtensorMap* mb = t.seg ? &tmB1 : &tmB0;
-        for (int kb = 0; kb < kbs; ++kb) {
-          if (!ptx::mbar_wait(&empty[stage], phase ^ 1, p.err)) {
-            set_error(p.err, kDevTimeoutProducer);
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&full[stage], kStage8);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          uint8_t* a_dst = sA + stage * kABytes8;
-          uint8_t* b_dst = sB + stage * kBBytes8;
-          const int k0 = kb * kBK8;
-          ptx::tma_load_2d(a_dst, ma, &full[stage], k0, t.row0);
-          if constexpr (EPI == Fp8Epi::kSwiGLU) {
-            int e, nrow;
-            if (t.seg == 0) {
-              e = t.group;
-              nrow = t.n * 128;
-            } else {
-              const int per = p.I / 128;
-              e = t.n / per;
-              nrow = (t.n % per) * 128;
+  if (warp < F8Cfg::kCtlWarps) {
+    // the register split is issued by whole warpgroups, ahead of each role's code
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F8Cfg::kCtlRegs));
+    if (warp == 0) {
+      // ================= TMA producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        for (int L = blockIdx.x; L < sch.total && ok; L += gridDim.x) {
+          const Tile t = sch.decode(L);
+          const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
+          const CUtensorMap* ma = t.seg ? &tmA1 : &tmA0;
+          const CUtensorMap* mb = t.seg ? &tmB1 : &tmB0;
+          for (int kb = 0; kb < kbs; ++kb) {
+            if (!ptx::mbar_wait(&empty[stage], phase ^ 1, p.err)) {
+              set_error(p.err, kDevTimeoutProducer);
+              ok = false;
+              break;
             }
-            ptx::tma_load_3d(b_dst + 0 * 8192, mb, &full[stage], k0, nrow, e);
-            ptx::tma_load_3d(b_dst + 1 * 8192, mb, &full[stage], k0, p.I + nrow, e);
-            ptx::tma_load_3d(b_dst + 2 * 8192, mb, &full[stage], k0, nrow + 64, e);
-            ptx::tma_load_3d(b_dst + 3 * 8192, mb, &full[stage], k0, p.I + nrow + 64, e);
-          } else {
-            if (t.seg == 0) {
-              ptx::tma_load_3d(b_dst, mb, &full[stage], k0, t.n * kBN8, t.group);
+            ptx::mbar_arrive_expect_tx(&full[stage], kStage8);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            uint8_t* a_dst = sA + stage * kABytes8;
+            uint8_t* b_dst = sB + stage * kBBytes8;
+            const int k0 = kb * kBK8;
+            ptx::tma_load_2d(a_dst, ma, &full[stage], k0, t.row0);
+            if constexpr (EPI == Fp8Epi::kSwiGLU) {
+              int e, nrow;
+              if (t.seg == 0) {
+                e = t.group;
+                nrow = t.n * 128;
+              } else {
+                const int per = p.I / 128;
+                e = t.n / per;
+                nrow = (t.n % per) * 128;
+              }
+              ptx::tma_load_3d(b_dst + 0 * 8192, mb, &full[stage], k0, nrow, e);
+              ptx::tma_load_3d(b_dst + 1 * 8192, mb, &full[stage], k0, p.I + nrow, e);
+              ptx::tma_load_3d(b_dst + 2 * 8192, mb, &full[stage], k0, nrow + 64, e);
+              ptx::tma_load_3d(b_dst + 3 * 8192, mb, &full[stage], k0, p.I + nrow + 64, e);
             } else {
-              ptx::tma_load_3d(b_dst, mb, &full[stage], k0 % p.I, t.n * kBN8, k0 / p.I);
+              if (t.seg == 0) {
+                ptx::tma_load_3d(b_dst, mb, &full[stage], k0, t.n * kBN8, t.group);
+              } else {
+                ptx::tma_load_3d(b_dst, mb, &full[stage], k0 % p.I, t.n * kBN8, k0 / p.I);
+              }
+            }
+            if (++stage == kStages8) {
+              stage = 0;
+              phase ^= 1;
             }
           }
-          if (++stage == kStages8) {
-            stage = 0;
-            phase ^= 1;
+        }
+        for (int s = 0; s < kStages8; ++s) {
+          if (armed & (1u << s)) {
+            if (!ptx::mbar_wait(&full[s], (armed_parity >> s) & 1u, nullptr)) set_error(p.err, kDevTimeoutDrain);
           }
         }
       }
-      for (int s = 0; s < kStages8; ++s) {
-        if (armed & (1u << s)) {
-          if (!ptx::mbar_wait(&full[s], (armed_parity >> s) & 1u, nullptr)) set_error(p.err, kDevTimeoutDrain);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ================= MMA issuer: one fresh accumulation per K block
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_e4m3(kBM, kBN8);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t g = 0;  // K blocks issued so far (selects the TMEM buffer)
-      bool ok = true;
-      for (int L = blockIdx.x; L < sch.total && ok; L += gridDim.x) {
-        const Tile t = sch.decode(L);
-        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
-        for (int kb = 0; kb < kbs; ++kb, ++g) {
-          const uint32_t b = g & 1;
-          if (!ptx::mbar_wait(&tempty[b], ((g >> 1) & 1) ^ 1, p.err) ||
-              !ptx::mbar_wait(&full[stage], phase, p.err)) {
-            set_error(p.err, kDevTimeoutMma);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t d_tmem = tmem_base + b * kBN8;
-          const uint64_t adesc = ptx::smem_desc_sw128(ptx::smem_u32(sA + stage * kABytes8));
-          const uint64_t bdesc = ptx::smem_desc_sw128(ptx::smem_u32(sB + stage * kBBytes8));
-#pragma unroll
-          for (int k = 0; k < kBK8 / kUK8; ++k) ptx::mma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0);
-          ptx::tc_commit(&empty[stage]);
-          ptx::tc_commit(&tfull[b]);
-          if (++stage == kStages8) {
-            stage = 0;
-            phase ^= 1;
+    } else if (warp == 1) {
+      // ================= MMA issuer: one fresh accumulation per K block
+      if (lane == 0) {
+        constexpr uint32_t idesc = ptx::idesc_e4m3(kBM, kBN8);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t g = 0;  // K blocks issued so far (selects the TMEM buffer)
+        bool ok = true;
+        for (int L = blockIdx.x; L < sch.total && ok; L += gridDim.x) {
+          const Tile t = sch.decode(L);
+          const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
+          for (int kb = 0; kb < kbs; ++kb, ++g) {
+            const uint32_t b = g & 1;
+            if (!ptx::mbar_wait(&tempty[b], ((g >> 1) & 1) ^ 1, p.err) ||
+                !ptx::mbar_wait(&full[stage], phase, p.err)) {
+              set_error(p.err, kDevTimeoutMma);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + b * kBN8;
+            const uint64_t adesc = ptx::smem_desc_sw128(ptx::smem_u32(sA + stage * kABytes8));
+            const uint64_t bdesc = ptx::smem_desc_sw128(ptx::smem_u32(sB + stage * kBBytes8));
+  #pragma unroll
+            for (int k = 0; k < kBK8 / kUK8; ++k) ptx::mma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0);
+            ptx::tc_commit(&empty[stage]);
+            ptx::tc_commit(&tfull[b]);
+            if (++stage == kStages8) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
+        ptx::tc_commit(mma_done);
+        if (!ptx::mbar_wait(mma_done, 0, nullptr)) set_error(p.err, kDevTimeoutDrain);
       }
-      ptx::tc_commit(mma_done);
-      if (!ptx::mbar_wait(mma_done, 0, nullptr)) set_error(p.err, kDevTimeoutDrain);
     }
   } else {
-    if constexpr (EPI == Fp8Epi::kSwiGLU) {
-      // ================= epilogue (warps 2..9)
-      const int q = warp & 3;
-      const int half = (warp - 2) >> 2;
-      const int r_in_tile = 32 * q + lane;
-      uint32_t g = 0;
-      bool ok = true;
-      for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
-        const Tile t = sch.decode(L);
-        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
-        const int row = t.row0 + r_in_tile;
-        const int rows_total = t.seg ? p.rows1 : p.rows_total0;
-        const bool valid = row < t.row_end;
-        const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
-        // per-tile weight-scale addressing
-        const float* sb_base;
-        int sb_stride_kb = 1;
-        int rb0 = 0, rb1 = 0;  // scale rows (128-row weight blocks) for this half's two 64-col parts
-        if constexpr (EPI == Fp8Epi::kSwiGLU) {
-          const int nblk = p.I / 128;  // 128-row blocks per projection
-          int e, nn;
-          if (t.seg == 0) {
-            e = t.group;
-            nn = t.n;
-          } else {
-            e = t.n / nblk;
-            nn = t.n % nblk;
-          }
-          const int kbk = t.seg ? p.k_blocks1 : p.k_blocks0;  // d / 128
-          sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbk;
-          rb0 = nn;          // gate block
-          rb1 = nblk + nn;   // up block
-          sb_stride_kb = kbk;
-        } else {
-          const int nbd = p.N / 128;  // d / 128 row blocks of W2
-          const int kpe = p.I / 128;  // K blocks per expert
-          sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
-          rb0 = rb1 = t.n * 2 + half;
-          sb_stride_kb = kpe;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F8Cfg::kEpiRegs));
+    // ================= epilogue (warps 4..11)
+    const int q = warp & 3;
+    const int half = (warp - F8Cfg::kCtlWarps) >> 2;  // columns 128 half .. 128 half + 127 of the tile
+    const int r_in_tile = 32 * q + lane;
+    uint8_t* stg = s_stage + (warp - F8Cfg::kCtlWarps) * kRowStageBytes;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
+      const Tile t = sch.decode(L);
+      const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
+      const int row = t.row0 + r_in_tile;
+      const int rows_total = t.seg ? p.rows1 : p.rows_total0;
+      const bool valid = row < t.row_end;
+      const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
+      // weight scales of this warp's columns: sb0p for the first 64, sb1p for
+      // the last 64, at offset kb (SwiGLU) or the block's place in [S, N/128, I/128]
+      const float* sb0p;
+      const float* sb1p;
+      int nbd = 0, kpe = 1;
+      if constexpr (EPI == Fp8Epi::kSwiGLU) {
+        // B tile rows [gate 0..63 | up 0..63 | gate 64..127 | up 64..127]:
+        // this half holds gate and up of h columns 64 half .. 64 half + 63
+        const int nblk = p.I / 128;  // 128-row blocks per projection
+        const int e = t.seg ? t.n / nblk : t.group;
+        const int nn = t.seg ? t.n % nblk : t.n;
+        const float* sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbs;
+        sb0p = sb_base + (size_t)nn * kbs;           // gate block
+        sb1p = sb_base + (size_t)(nblk + nn) * kbs;  // up block
+      } else {
+        // down projection: K runs over S experts of I columns each in the
+        // shared segment, over one expert's I in the routed one
+        nbd = p.N / 128;
+        kpe = p.I / 128;
+        const float* sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
+        sb0p = sb1p = sb_base + (size_t)(t.n * 2 + half) * kpe;
+      }
+      auto sb_off = [&](int kb) -> int {
+        if constexpr (EPI == Fp8Epi::kSwiGLU) return kb;
+        else return (kb / kpe) * nbd * kpe + kb % kpe;
+      };
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      // the scales of block kb + 1 are loaded while block kb drains
+      const bool row_in = row < rows_total;
+      float sa_n = 0.0f, sb0_n = 0.0f, sb1_n = 0.0f;
+      if (kbs > 0) {
+        sa_n = row_in ? __ldg(sa_base + row) : 0.0f;
+        sb0_n = __ldg(sb0p);
+        sb1_n = EPI == Fp8Epi::kSwiGLU ? __ldg(sb1p) : sb0_n;
+      }
+      for (int kb = 0; kb < kbs; ++kb, ++g) {
+        const uint32_t b = g & 1;
+        const float f0 = sa_n * sb0_n, f1 = sa_n * sb1_n;
+        if (kb + 1 < kbs) {
+          const int o = sb_off(kb + 1);
+          sa_n = row_in ? __ldg(sa_base + (size_t)(kb + 1) * rows_total + row) : 0.0f;
+          sb0_n = __ldg(sb0p + o);
+          sb1_n = EPI == Fp8Epi::kSwiGLU ? __ldg(sb1p + o) : sb0_n;
         }
-        float acc[128];
-  #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-        for (int kb = 0; kb < kbs; ++kb, ++g) {
-          const uint32_t b = g & 1;
-          if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
-            set_error(p.err, kDevTimeoutEpilogue);
-            ok = false;
-          }
-          ptx::tc_fence_after();
-          const float sa = (row < rows_total && ok) ? __ldg(sa_base + (size_t)kb * rows_total + row) : 0.0f;
-          float f0, f1;
-          if constexpr (EPI == Fp8Epi::kSwiGLU) {
-            f0 = sa * __ldg(sb_base + (size_t)rb0 * sb_stride_kb + kb);
-            f1 = sa * __ldg(sb_base + (size_t)rb1 * sb_stride_kb + kb);
-          } else {
-            // shared segment: K runs over S experts of I columns each
-            const int e = t.seg ? (kb * 128) / p.I : 0;
-            const int kk = t.seg ? ((kb * 128) % p.I) / 128 : kb;
-            const float* sb = t.seg ? p.b_scale1 + (size_t)e * (p.N / 128) * (p.I / 128) : sb_base;
-            f0 = f1 = sa * __ldg(sb + (size_t)rb0 * sb_stride_kb + kk);
-          }
-          if (ok) {
-            const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8 + half * 128;
-  #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float v[32];
-              ptx::tmem_ld32(tb + c * 32, v);
-              const float f = (c < 2) ? f0 : f1;
-  #pragma unroll
-              for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(v[j], f, acc[c * 32 + j]);
-            }
-          }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+        if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
+          set_error(p.err, kDevTimeoutEpilogue);
+          ok = false;
         }
-        if constexpr (EPI == Fp8Epi::kSwiGLU) {
-          // h = silu(gate) * up for this half's 64 intermediate columns, then the
-          // 1x128 e4m3 tile shared with the other half of the row
-          float amax = 0.0f;
-  #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            acc[j] = silu(acc[j]) * acc[64 + j];
-            amax = fmaxf(amax, fabsf(acc[j]));
+        ptx::tc_fence_after();
+        float v0[32], v1[32];
+        const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8 + half * 128;
+        if (ok) {
+          // columns 0..63 of this half, two loads in flight
+          ptx::tmem_ld32_nowait(tb, v0);
+          ptx::tmem_ld32_nowait(tb + 32, v1);
+          ptx::tmem_wait_ld(v0);
+          ptx::tmem_wait_ld(v1);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            acc[j] = fmaf(v0[j], f0, acc[j]);
+            acc[32 + j] = fmaf(v1[j], f0, acc[32 + j]);
           }
-          s_amax[half * 128 + r_in_tile] = amax;
-          epi_bar();
-          amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + r_in_tile]);
-          epi_bar();  // s_amax is rewritten by the next tile
-          const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-          if (valid) {
-            uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
-            const int ldo = t.seg ? p.ldo1 : p.ldo0;
-            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + half * 64);
-  #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
-                               __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
-              w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
-                               __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
-              w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
-                               __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
-              w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
-                               __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
-              dst[v] = w;
-            }
-            if (half == 0) {
-              float* hs = t.seg ? p.out_scale1 : p.out_scale0;
-              hs[(size_t)t.n * rows_total + row] = scale;
-            }
-          }
-        } else {
-          if (valid) {
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
-            const int ldo = t.seg ? p.ldo1 : p.ldo0;
-            const size_t o = (size_t)row * ldo + t.n * kBN8 + half * 128;
-  #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
-              store_bf16x32(out + o + 32 * c, acc + 32 * c);
-            }
+          // columns 64..127; the buffer is released before their FMAs
+          ptx::tmem_ld32_nowait(tb + 64, v0);
+          ptx::tmem_ld32_nowait(tb + 96, v1);
+          ptx::tmem_wait_ld(v0);
+          ptx::tmem_wait_ld(v1);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            acc[64 + j] = fmaf(v0[j], f1, acc[64 + j]);
+            acc[96 + j] = fmaf(v1[j], f1, acc[96 + j]);
           }
         }
       }
-    } else {
-      // ================= epilogue (warps 2..17)
-      const int q = warp & 3;
-      const int slice = (warp - 2) >> 2;  // 0..3
-      const int r_in_tile = 32 * q + lane;
-      // SwiGLU: this warp's 32 h columns are 32 slice .. 32 slice + 31 of the
-      // tile's 128; their gate accumulators start at column ga (B tile rows are
-      // [gate 0..63 | up 0..63 | gate 64..127 | up 64..127]), the up ones at ga + 64
-      const int ga = slice < 2 ? 32 * slice : 128 + 32 * (slice - 2);
-      uint32_t g = 0;
-      bool ok = true;
-      for (int L = blockIdx.x; L < sch.total; L += gridDim.x) {
-        const Tile t = sch.decode(L);
-        const int kbs = t.seg ? p.k_blocks1 : p.k_blocks0;
-        const int row = t.row0 + r_in_tile;
-        const int rows_total = t.seg ? p.rows1 : p.rows_total0;
-        const bool valid = row < t.row_end;
-        const float* sa_base = t.seg ? p.a_scale1 : p.a_scale0;
-        // per-tile weight-scale addressing
-        const float* sb_base;
-        int sb_stride_kb = 1;
-        int rb0 = 0, rb1 = 0;  // scale rows (128-row weight blocks) of this warp's two 32-column parts
-        if constexpr (EPI == Fp8Epi::kSwiGLU) {
-          const int nblk = p.I / 128;  // 128-row blocks per projection
-          int e, nn;
-          if (t.seg == 0) {
-            e = t.group;
-            nn = t.n;
-          } else {
-            e = t.n / nblk;
-            nn = t.n % nblk;
-          }
-          const int kbk = t.seg ? p.k_blocks1 : p.k_blocks0;  // d / 128
-          sb_base = (t.seg ? p.b_scale1 : p.b_scale0) + (size_t)e * (2 * nblk) * kbk;
-          rb0 = nn;          // gate block
-          rb1 = nblk + nn;   // up block
-          sb_stride_kb = kbk;
-        } else {
-          const int nbd = p.N / 128;  // d / 128 row blocks of W2
-          const int kpe = p.I / 128;  // K blocks per expert
-          sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
-          rb0 = rb1 = t.n * 2 + (slice >> 1);  // columns 64 slice .. 64 slice + 63
-          sb_stride_kb = kpe;
+      if constexpr (EPI == Fp8Epi::kSwiGLU) {
+        // h = silu(gate) * up for this half's 64 intermediate columns, then the
+        // 1x128 e4m3 tile shared with the other half of the row
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          acc[j] = silu(acc[j]) * acc[64 + j];
+          amax = fmaxf(amax, fabsf(acc[j]));
         }
-        float acc[64];
-  #pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-        for (int kb = 0; kb < kbs; ++kb, ++g) {
-          const uint32_t b = g & 1;
-          if (ok && !ptx::mbar_wait(&tfull[b], (g >> 1) & 1, p.err)) {
-            set_error(p.err, kDevTimeoutEpilogue);
-            ok = false;
+        s_amax[half * 128 + r_in_tile] = amax;
+        epi_bar();
+        amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + r_in_tile]);
+        epi_bar();  // s_amax is rewritten by the next tile
+        const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        if (valid) {
+          uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
+          const int ldo = t.seg ? p.ldo1 : p.ldo0;
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + half * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
+                             __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
+            w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
+                             __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
+            w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
+                             __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
+            w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
+                             __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
+            dst[v] = w;
           }
-          ptx::tc_fence_after();
-          const float sa = (row < rows_total && ok) ? __ldg(sa_base + (size_t)kb * rows_total + row) : 0.0f;
-          float f0, f1;
-          if constexpr (EPI == Fp8Epi::kSwiGLU) {
-            f0 = sa * __ldg(sb_base + (size_t)rb0 * sb_stride_kb + kb);
-            f1 = sa * __ldg(sb_base + (size_t)rb1 * sb_stride_kb + kb);
-          } else {
-            // shared segment: K runs over S experts of I columns each
-            const int e = t.seg ? (kb * 128) / p.I : 0;
-            const int kk = t.seg ? ((kb * 128) % p.I) / 128 : kb;
-            const float* sb = t.seg ? p.b_scale1 + (size_t)e * (p.N / 128) * (p.I / 128) : sb_base;
-            f0 = f1 = sa * __ldg(sb + (size_t)rb0 * sb_stride_kb + kk);
+          if (half == 0) {
+            float* hs = t.seg ? p.out_scale1 : p.out_scale0;
+            hs[(size_t)t.n * rows_total + row] = scale;
           }
-          if (ok) {
-            const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + b * kBN8;
-            const uint32_t c0 = EPI == Fp8Epi::kSwiGLU ? ga : 64 * slice;
-            const uint32_t c1 = EPI == Fp8Epi::kSwiGLU ? ga + 64 : 64 * slice + 32;
-            // 16 columns per load keeps the temporaries within the 96
-            // registers a thread of a 576-thread block has
-  #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float v[16];
-              ptx::tmem_ld16(tb + (h < 2 ? c0 : c1) + 16 * (h & 1), v);
-              const float f = h < 2 ? f0 : f1;
-  #pragma unroll
-              for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(v[j], f, acc[16 * h + j]);
-            }
-          }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty[b]);
         }
-        if constexpr (EPI == Fp8Epi::kSwiGLU) {
-          // h = silu(gate) * up for this warp's 32 intermediate columns, then
-          // the 1x128 e4m3 tile shared with the three other slices of the row
-          float amax = 0.0f;
-  #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            acc[j] = silu(acc[j]) * acc[32 + j];
-            amax = fmaxf(amax, fabsf(acc[j]));
+      } else {
+        // bf16 rows through the warp's staging block, 32 columns at a time
+        // (kCombine adds the routed sum of the row first)
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
+        const int ldo = t.seg ? p.ldo1 : p.ldo0;
+        const int rbase = t.row0 + 32 * q;
+        const int nrows = max(0, min(32, t.row_end - rbase));
+        const size_t col = (size_t)t.n * kBN8 + half * 128;
+        uint8_t* base = reinterpret_cast<uint8_t*>(out + (size_t)rbase * ldo + col);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if constexpr (EPI == Fp8Epi::kCombine) {
+            if (valid) add_bf16x32(acc + 32 * c, p.radd + (size_t)row * ldo + col + 32 * c, 1.0f);
           }
-          s_amax[slice * 128 + r_in_tile] = amax;
-          epi_bar();
-  #pragma unroll
-          for (int o = 0; o < 4; ++o) amax = fmaxf(amax, s_amax[o * 128 + r_in_tile]);
-          epi_bar();  // s_amax is rewritten by the next tile
-          const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-          if (valid) {
-            uint8_t* out = static_cast<uint8_t*>(t.seg ? p.out1 : p.out0);
-            const int ldo = t.seg ? p.ldo1 : p.ldo0;
-            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + t.n * 128 + slice * 32);
-  #pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              uint4 w;
-              w.x = pack4_e4m3(__fdiv_rn(acc[16 * v + 0], scale), __fdiv_rn(acc[16 * v + 1], scale),
-                               __fdiv_rn(acc[16 * v + 2], scale), __fdiv_rn(acc[16 * v + 3], scale));
-              w.y = pack4_e4m3(__fdiv_rn(acc[16 * v + 4], scale), __fdiv_rn(acc[16 * v + 5], scale),
-                               __fdiv_rn(acc[16 * v + 6], scale), __fdiv_rn(acc[16 * v + 7], scale));
-              w.z = pack4_e4m3(__fdiv_rn(acc[16 * v + 8], scale), __fdiv_rn(acc[16 * v + 9], scale),
-                               __fdiv_rn(acc[16 * v + 10], scale), __fdiv_rn(acc[16 * v + 11], scale));
-              w.w = pack4_e4m3(__fdiv_rn(acc[16 * v + 12], scale), __fdiv_rn(acc[16 * v + 13], scale),
-                               __fdiv_rn(acc[16 * v + 14], scale), __fdiv_rn(acc[16 * v + 15], scale));
-              dst[v] = w;
-            }
-            if (slice == 0) {
-              float* hs = t.seg ? p.out_scale1 : p.out_scale0;
-              hs[(size_t)t.n * rows_total + row] = scale;
-            }
-          }
-        } else {
-          if (valid) {
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.seg ? p.out1 : p.out0);
-            const int ldo = t.seg ? p.ldo1 : p.ldo0;
-            const size_t o = (size_t)row * ldo + t.n * kBN8 + slice * 64;
-  #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              if constexpr (EPI == Fp8Epi::kCombine) add_bf16x32(acc + 32 * c, p.radd + o + 32 * c, 1.0f);
-              store_bf16x32(out + o + 32 * c, acc + 32 * c);
-            }
-          }
+          uint4 w[4];
+          pack_bf16x32(acc + 32 * c, w);
+          warp_store_rows64(stg, lane, w, base + c * 64, (size_t)ldo * 2, nrows);
         }
       }
     }
@@ -519,7 +426,19 @@ cudaError_t launch_fp8_one(const Fp8GemmLaunch& L) {
   static int attr_done[64] = {};
   cudaError_t e = set_smem_once(kern, kSmem8, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, F8Cfg<EPI>::kThreads, kSmem8, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
+  {
+    // setmaxnreg.inc waits until the registers it asks for are free: refuse
+    // to launch unless the block starts with exactly the registers it splits
+    static int regs_ok = 0;
+    if (!regs_ok) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != F8Cfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
+      regs_ok = 1;
+    }
+  }
+  kern<<<L.grid, F8Cfg::kThreads, kSmem8, L.stream>>>(L.a0, L.b0, L.a1, L.b1, L.p);
   return cudaGetLastError();
 }
 
