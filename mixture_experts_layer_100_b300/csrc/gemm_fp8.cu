@@ -332,9 +332,9 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
           ptx::tmem_wait_ld(v0);
           ptx::tmem_wait_ld(v1);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            acc[j] = fmaf(v0[j], f0, acc[j]);
-            acc[32 + j] = fmaf(v1[j], f0, acc[32 + j]);
+          for (int j = 0; j < 32; j += 2) {
+            ptx::ffma2(acc[j], acc[j + 1], v0[j], v0[j + 1], f0);
+            ptx::ffma2(acc[32 + j], acc[33 + j], v1[j], v1[j + 1], f0);
           }
           // columns 64..127; the buffer is released before their FMAs
           ptx::tmem_ld32_nowait(tb + 64, v0);
@@ -347,9 +347,9 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&tempty[b]);
         if (ok) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            acc[64 + j] = fmaf(v0[j], f1, acc[64 + j]);
-            acc[96 + j] = fmaf(v1[j], f1, acc[96 + j]);
+          for (int j = 0; j < 32; j += 2) {
+            ptx::ffma2(acc[64 + j], acc[65 + j], v0[j], v0[j + 1], f1);
+            ptx::ffma2(acc[96 + j], acc[97 + j], v1[j], v1[j + 1], f1);
           }
         }
       }

@@ -274,5 +274,14 @@ __device__ __forceinline__ void tmem_wait_ld(float* v) {
                : "memory");
 }
 
+// d0 += a0 * b, d1 += a1 * b as one packed fp32x2 FMA (each lane rounded
+// like fmaf): half the issue slots of two scalar FMAs.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b) {
+  asm("{\n\t.reg .b64 d, a, s;\n\tmov.b64 d, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+      "fma.rn.f32x2 d, a, s, d;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b));
+}
+
 }  // namespace ptx
 }  // namespace moe
