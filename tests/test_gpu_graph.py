@@ -27,11 +27,13 @@ def _call(B, cfg, x, W, bias, gamma, o, ws):
 
 @pytest.mark.parametrize("name,expert", [("mid_t4096_d2048_e64_bf16", None),
                                          ("t515_d512_e32_s2_ue8m0", "e4m3_ue8m0"),
+                                         ("t515_d512_e32_s2_e4m3", "e4m3"),
                                          ("t300_d256_e16_f32", "f32")])
 def test_graph_replay_matches_eager_steps(name, expert):
     from mixture_experts_layer_100_b300 import binding as B
-    if name == "t515_d512_e32_s2_ue8m0":
-        p = synth.PRESETS["v3_t32768_d7168_e256_fp8_ue8m0"].replace(
+    if name in ("t515_d512_e32_s2_ue8m0", "t515_d512_e32_s2_e4m3"):
+        base = "v3_t32768_d7168_e256_fp8_ue8m0" if expert == "e4m3_ue8m0" else "v3_t32768_d7168_e256_fp8"
+        p = synth.PRESETS[base].replace(
             name=name, T=515, d=512, E=32, G=8, K=6, M=3, I=384, S=2, zipf=False, bias="u0.02")
     elif name == "t300_d256_e16_f32":
         p = synth.PRESETS["tiny_t256_d512_e16_fp32"].replace(name=name, T=300, d=256, bias="u0.02")
@@ -40,8 +42,8 @@ def test_graph_replay_matches_eager_steps(name, expert):
     w = synth.make_weights(p, device=DEV)
     x = synth.make_x(p, w.w_router, device=DEV)
     wd = device_weights(w)
-    if expert == "e4m3_ue8m0":
-        wd = quantize_device_weights(wd, ue8m0=True)
+    if expert in ("e4m3", "e4m3_ue8m0"):
+        wd = quantize_device_weights(wd, ue8m0=expert == "e4m3_ue8m0")
     W = B.make_weights(**wd)
     cfg = B.config_from_preset(p)
     b0 = synth.make_bias(p, device=DEV)
