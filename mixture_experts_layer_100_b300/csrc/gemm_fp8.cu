@@ -299,10 +299,10 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
         const float* sb_base = t.seg ? p.b_scale1 : p.b_scale0 + (size_t)t.group * nbd * kpe;
         sb0p = sb1p = sb_base + (size_t)(t.n * 2 + half) * kpe;
       }
-      auto sb_off = [&](int kb) -> int {
-        if constexpr (EPI == Fp8Epi::kSwiGLU) return kb;
-        else return (kb / kpe) * nbd * kpe + kb % kpe;
-      };
+      // offset of the next block's weight scale: kb (SwiGLU); in the down
+      // projections the K block within an expert, plus nbd * kpe per expert
+      // passed (stepped, not divided, per block)
+      int sb_k = 0, sb_e = 0;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
@@ -318,7 +318,16 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
         const uint32_t b = g & 1;
         const float f0 = sa_n * sb0_n, f1 = sa_n * sb1_n;
         if (kb + 1 < kbs) {
-          const int o = sb_off(kb + 1);
+          int o;
+          if constexpr (EPI == Fp8Epi::kSwiGLU) {
+            o = kb + 1;
+          } else {
+            if (++sb_k == kpe) {
+              sb_k = 0;
+              sb_e += nbd * kpe;
+            }
+            o = sb_e + sb_k;
+          }
           sa_n = row_in ? __ldg(sa_base + (size_t)(kb + 1) * rows_total + row) : 0.0f;
           sb0_n = __ldg(sb0p + o);
           sb1_n = EPI == Fp8Epi::kSwiGLU ? __ldg(sb1p + o) : sb0_n;
