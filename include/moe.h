@@ -247,9 +247,12 @@ moe_status moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, co
  * calling thread records events[i] (cudaEvent_t handles owned by the caller)
  * on its stream at stage boundary i: 0 before the router, 1 after the router
  * GEMM, 2 after the top-K selection, 3 after the permutation, 4 after the
- * expert GEMM1 (SwiGLU, routed and shared experts in one launch), 5 after the
- * routed down projection, 6 after the shared down projection with the fused
- * combine, 7 after the bias update. count must be 0 (hook off) or >= 8. */
+ * routed experts' GEMM1 (SwiGLU), 5 after the routed down projection, 6 after
+ * the shared down projection with the fused combine, 7 after the bias update.
+ * The shared experts' GEMM1 runs on a side stream from mark 1 on and is
+ * joined before the shared down projection (between marks 5 and 6), so the
+ * stages in between share the GPU with it. count must be 0 (hook off) or
+ * >= 8. */
 moe_status moe_set_stage_events(void* const* events, int count);
 
 /* Self-test of the device-side wait bound: queues one small kernel that waits

@@ -267,10 +267,9 @@ moe_status moe_set_stage_events(void* const* events, int count) {
     return MOE_OK;
   }
   if (events == nullptr || count < 8) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < 8; ++i) {
-    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
-    g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
-  }
+  for (int i = 0; i < 8; ++i)
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;  // the previous hook stays as it was
+  for (int i = 0; i < 8; ++i) g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
   g_stage_on = true;
   return MOE_OK;
 }

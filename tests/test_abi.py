@@ -88,3 +88,41 @@ def test_null_pointers_rejected_before_any_cuda_call():
     st = B.lib.moe_bias_update(ctypes.byref(cfg), ctypes.c_void_p(0x1004), ctypes.c_float(1e-3),
                                ctypes.c_void_p(0x2000), None, None)
     assert st == 1
+
+
+def test_newer_entry_points_reject_bad_arguments_before_any_cuda_call():
+    cfg = B.make_config(T=8, d=512, E=16, G=4, K=4, M=2, I=256, S=1, act="f32")
+    f = ctypes.c_float
+    # sequence-wise balance statistic: seq_len must be positive; indices and loss are required
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg), ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), 0, f(1.0),
+                                 ctypes.c_void_p(0x3000), None, None, None, None) == 1
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg), ctypes.c_void_p(0x1000), None, 4, f(1.0),
+                                 ctypes.c_void_p(0x3000), None, None, None, None) == 1
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg), ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), 4, f(1.0),
+                                 None, None, None, None, None) == 1
+    # scores taken from the workspace need a workspace
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg), None, ctypes.c_void_p(0x2000), 4, f(1.0),
+                                 ctypes.c_void_p(0x3000), None, None, None, None) == 1
+    # misaligned f / p outputs
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg), ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), 4, f(1.0),
+                                 ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4002), None, None, None) == 1
+    # T = 0: nothing to do
+    cfg0 = B.make_config(T=0, d=512, E=16, G=4, K=4, M=2, I=256, S=1, act="f32")
+    assert B.lib.moe_seq_balance(ctypes.byref(cfg0), None, None, 4, f(1.0), None, None, None, None, None) == 0
+    # weight quantisers: negative sizes, missing buffers; empty is a no-op
+    for q in (B.lib.moe_quantize_weights_e4m3, B.lib.moe_quantize_weights_e4m3_ue8m0):
+        assert q(ctypes.c_void_p(0x1000), -1, 128, 128, ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), None) == 1
+        assert q(None, 1, 128, 128, ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), None) == 1
+        assert q(ctypes.c_void_p(0x1000), 1, 128, 128, ctypes.c_void_p(0x2000), None, None) == 1
+        assert q(None, 0, 128, 128, None, None, None) == 0
+    # stage-event hook: off is fine, fewer than 8 events or a null array is not
+    assert B.lib.moe_set_stage_events(None, 0) == 0
+    assert B.lib.moe_set_stage_events(None, 8) == 1
+    arr = (ctypes.c_void_p * 4)(*([0x10] * 4))
+    assert B.lib.moe_set_stage_events(arr, 4) == 1
+    arr8 = (ctypes.c_void_p * 8)(*([0x10] * 7 + [None]))
+    assert B.lib.moe_set_stage_events(arr8, 8) == 1
+    # device error query needs a workspace and an output
+    code = ctypes.c_int(0)
+    assert B.lib.moe_device_error(None, None, ctypes.byref(code)) == 1
+    assert B.lib.moe_device_error(ctypes.c_void_p(0x1000), None, None) == 1
