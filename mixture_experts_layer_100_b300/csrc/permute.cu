@@ -109,11 +109,34 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
     const VecT* src = x + (size_t)t * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) {
-      const VecT val = src[i];
-      for (int k = 0; k < K; ++k) {
-        const int pk = __shfl_sync(0xffffffffu, pos, k);
-        if (pk >= 0) xp[(size_t)pk * row_vecs + i] = val;
+    if (K <= 8) {
+      // positions fetched once per token; four loads per lane in flight
+      // before their stores (the copy is bound by bytes in flight)
+      int pk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pk[k] = __shfl_sync(0xffffffffu, pos, k);
+      for (int i0 = lane; i0 < row_vecs; i0 += 4 * 32) {
+        VecT v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i0 + 32 * u < row_vecs) v[u] = src[i0 + 32 * u];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k < K && pk[k] >= 0) {
+            VecT* dst = xp + (size_t)pk[k] * row_vecs;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (i0 + 32 * u < row_vecs) dst[i0 + 32 * u] = v[u];
+          }
+        }
+      }
+    } else {
+      for (int i = lane; i < row_vecs; i += 32) {
+        const VecT val = src[i];
+        for (int k = 0; k < K; ++k) {
+          const int pk = __shfl_sync(0xffffffffu, pos, k);
+          if (pk >= 0) xp[(size_t)pk * row_vecs + i] = val;
+        }
       }
     }
   }
