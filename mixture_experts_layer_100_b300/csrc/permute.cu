@@ -171,42 +171,64 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    // two tiles per warp iteration: lanes 0..15 tile 2i, lanes 16..31 tile 2i+1
-    for (int tile0 = 0; tile0 < ntiles; tile0 += 2) {
-      const int tile = tile0 + (lane >> 4);
-      const bool act = tile < ntiles;
-      float f[8];
-      float amax = 0.0f;
-      if (act) {
-        const uint4 w = src[tile * 16 + (lane & 15)];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+    // the K positions fetched once per token (K <= 8)
+    int pks[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 v = __bfloat1622float2(h[j]);
-          f[2 * j] = v.x;
-          f[2 * j + 1] = v.y;
+    for (int k = 0; k < 8; ++k) pks[k] = __shfl_sync(0xffffffffu, pos, k);
+    // four tiles per warp iteration, both loads issued first: lanes 0..15
+    // take tiles 4i and 4i+2, lanes 16..31 tiles 4i+1 and 4i+3
+    for (int tile00 = 0; tile00 < ntiles; tile00 += 4) {
+      uint4 wv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int tl = tile00 + 2 * u + (lane >> 4);
+        if (tl < ntiles) wv[u] = src[tl * 16 + (lane & 15)];
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int tile0 = tile00 + 2 * u;
+        const int tile = tile0 + (lane >> 4);
+        const bool act = tile < ntiles;
+        float f[8];
+        float amax = 0.0f;
+        if (act) {
+          const uint4 w = wv[u];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 v = __bfloat1622float2(h[j]);
+            f[2 * j] = v.x;
+            f[2 * j + 1] = v.y;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-      }
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = e4m3_tile_scale(amax, ue8m0);
+        uint2 packed = make_uint2(0, 0);
+        if (act) {
+          uint32_t lo = 0, hi = 0;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = e4m3_tile_scale(amax, ue8m0);
-      uint2 packed = make_uint2(0, 0);
-      if (act) {
-        uint32_t lo = 0, hi = 0;
+          for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], scale)) << (8 * j);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], scale)) << (8 * j);
+          for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], scale)) << (8 * j);
+          packed = make_uint2(lo, hi);
+        }
+        if (K <= 8) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], scale)) << (8 * j);
-        packed = make_uint2(lo, hi);
+          for (int k = 0; k < 8; ++k)
+            if (k < K && act && pks[k] >= 0)
+              reinterpret_cast<uint2*>(xp + (size_t)pks[k] * d + tile * 128)[lane & 15] = packed;
+        } else {
+          for (int k = 0; k < K; ++k) {
+            const int pk = __shfl_sync(0xffffffffu, pos, k);
+            if (act && pk >= 0) reinterpret_cast<uint2*>(xp + (size_t)pk * d + tile * 128)[lane & 15] = packed;
+          }
+        }
+        if (act && (lane & 15) == 0) tok_scale[(size_t)t * ntiles + tile] = scale;
+        if (act && xq != nullptr) reinterpret_cast<uint2*>(xq + (size_t)t * d + tile * 128)[lane & 15] = packed;
       }
-      for (int k = 0; k < K; ++k) {
-        const int pk = __shfl_sync(0xffffffffu, pos, k);
-        if (act && pk >= 0) reinterpret_cast<uint2*>(xp + (size_t)pk * d + tile * 128)[lane & 15] = packed;
-      }
-      if (act && (lane & 15) == 0) tok_scale[(size_t)t * ntiles + tile] = scale;
-      if (act && xq != nullptr) reinterpret_cast<uint2*>(xq + (size_t)t * d + tile * 128)[lane & 15] = packed;
     }
   }
 }
