@@ -57,7 +57,7 @@ typedef struct CUstream_st* moe_stream_t;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,  /* bad pointer, shape or combination */
-  MOE_ERR_UNSUPPORTED = 2,  /* valid layer, but a shape this build does not run */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid layer, but a shape the library does not run */
   MOE_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
   MOE_ERR_TIMEOUT = 4,      /* a device-side wait ran out (see moe_device_error) */
   MOE_ERR_DEVICE = 5        /* device-side check failed (see moe_device_error) */

@@ -54,7 +54,7 @@ def test_workspace_size_presets(name):
     ("K", 9, 1),           # K > M * E / G  (E=16, G=4, M=2)
     ("group_topk", 5, 1),  # group_topk > E / G
     ("G", 64, 1),          # E % G
-    ("E", 1024, 2),        # too many experts for this build (G divides)
+    ("E", 1024, 2),        # more experts than the library supports (G divides)
     ("T", -1, 1),
 ])
 def test_invalid_configs(field, value, status):
