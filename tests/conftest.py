@@ -28,8 +28,12 @@ def pytest_collection_modifyitems(config, items):
 
 
 def pytest_sessionstart(session):
-    """Build the CUDA library in-tree if a source is newer than the .so."""
+    """Build the CUDA library and the C++ oracle in-tree if a source is newer
+    than its .so."""
     from mixture_experts_layer_100_b300 import build
+    from oracle import build as oracle_build
 
     if build.needs_build():
         build.build()
+    if oracle_build.needs_build():
+        oracle_build.build()
