@@ -35,6 +35,7 @@ from mixture_experts_layer_100_b300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/sec (1×B300, V3 shape T=16K bf16); % tensor/HBM roofline"
 DEFAULT_PRESET = "v3_t16384_d7168_e256_bf16"
+L2_BYTES = 126 * 2 ** 20
 STAGES = ["router_gemm", "route_select", "permute", "gemm1_swiglu", "gemm2_routed", "gemm2_shared_combine",
           "bias_update"]
 
@@ -55,6 +56,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-standalone", action="store_true",
                     help="skip the standalone timing of moe_route / moe_permute")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode-shape and FP8 workloads timed after the V3 bf16 headline")
     return ap.parse_args()
 
 
@@ -201,52 +204,75 @@ def hbm_bytes(p):
 
 # ---------------------------------------------------------------- CPU oracle leg
 class CpuOracleUnit:
-    """One bounded unit of the workload run by the CPU oracle: routing of an
-    `nt`-token block, and the SwiGLU FFN of `rows` rows on each of
-    `n_experts` experts. Host copies of the inputs are made once, untimed."""
+    """One bounded unit of the workload run by the C++ CPU oracle
+    (oracle/moe_oracle.cpp, plain loops in double, g++ -O2) on the host cores:
+    the routing of a block of `nt` tokens (router GEMM and sigmoid,
+    group-limited top-K, load count, bias update) and the SwiGLU FFN of the
+    block's first `rows` tokens on two experts (the first shared expert, or
+    routed expert 0 when S = 0, and the routed expert E/2), in the workload's
+    expert precision. Tokens/s is extrapolated as
+    1 / (t_route / nt + (K + S) * t_ffn / (2 * rows)): every token runs K
+    routed and S shared expert FFNs of the same cost. Both the bench line's
+    cpu_baseline and the reference arm time this unit. Host copies of the
+    inputs are made once, untimed."""
 
-    def __init__(self, p, w, x_host, nt=2048, rows=512, n_experts=2):
+    def __init__(self, p, w, x_host, nt=4096, rows=128):
         import numpy as np
         self.p = p
         self.nt = min(nt, p.T)
-        self.rows = min(rows, p.T)
-        self.xb = x_host[:self.nt].float().numpy()
+        self.rows = min(rows, self.nt)
+        self.xb = np.ascontiguousarray(x_host[:self.nt].float().numpy())
         self.wr = w.w_router.float().cpu().numpy()
-        self.b = np.zeros(p.E, np.float32)
-        experts = [(i * p.E) // n_experts for i in range(n_experts)]
-        self.ew = [(w.w13[e].float().cpu().numpy(), w.w2[e].float().cpu().numpy()) for e in experts]
-        self.desc = (f"oracle routing of {self.nt} tokens + oracle SwiGLU FFN of {self.rows} rows on "
-                     f"{n_experts} expert(s), extrapolated to K+S={p.K + p.S} expert rows per token")
+        self.b = synth.make_bias(p).numpy()
+        first = (w.ws13[0], w.ws2[0]) if p.S > 0 else (w.w13[0], w.w2[0])
+        self.ew = [(first[0].float().cpu().numpy(), first[1].float().cpu().numpy()),
+                   (w.w13[p.E // 2].float().cpu().numpy(), w.w2[p.E // 2].float().cpu().numpy())]
+        self.f8 = p.expert_dtype in ("e4m3", "e4m3_ue8m0")
+        self.desc = (f"C++ oracle: routing + load count + bias update of {self.nt} tokens, and the "
+                     f"{p.expert_dtype} SwiGLU FFN of {self.rows} tokens on 2 experts, extrapolated to "
+                     f"K+S={p.K + p.S} expert FFNs per token")
 
     def run(self):
         """Returns (tokens/s extrapolated to the whole layer, seconds)."""
-        from oracle import moe_oracle as om
+        import numpy as np
+        from oracle import cpp
         p = self.p
         t0 = time.perf_counter()
-        s = om.router_scores(self.xb, self.wr)
-        om.select_experts(s, self.b, p.G, p.K, p.M, p.group_topk)
+        s = cpp.router_scores(self.xb, self.wr)
+        idx, _ = cpp.select_experts(s, self.b, p.G, p.K, p.M, p.group_topk)
+        cpp.bias_update(cpp.expert_counts(idx, p.E), self.b, p.gamma, self.nt, p.K)
         t1 = time.perf_counter()
+        acc = np.zeros((self.rows, p.d))
         for w13, w2 in self.ew:
-            om.swiglu_ffn(self.xb[:self.rows], w13, w2)
+            cpp.expert_accumulate(self.xb[:self.rows], np.arange(self.rows), w13, w2, None, acc, fp8=self.f8,
+                                  ue8m0=p.expert_dtype == "e4m3_ue8m0")
         t2 = time.perf_counter()
         per_tok = (t1 - t0) / self.nt + (p.K + p.S) * (t2 - t1) / (len(self.ew) * self.rows)
         return 1.0 / per_tok, t2 - t0
 
     @staticmethod
     def cores():
-        """Threads the oracle's BLAS runs on (all cores this process may use
-        unless a thread-pool limit says otherwise)."""
-        try:
-            from threadpoolctl import threadpool_info
-            blas = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-            if blas:
-                return max(blas)
-        except ImportError:
-            pass
-        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-            if os.environ.get(var, "").isdigit():
-                return int(os.environ[var])
-        return len(os.sched_getaffinity(0))
+        """Threads the C++ oracle runs on: std::thread::hardware_concurrency()."""
+        from oracle import cpp
+        return cpp.hardware_threads()
+
+
+def bench_config(p, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": p.name, "T": p.T, "d": p.d, "E": p.E, "G": p.G, "K": p.K, "M": p.M, "I": p.I, "S": p.S,
+            "gamma": p.gamma, "global_tokens_per_step": p.T * world,
+            "parallelism": f"dp{world} replicas" if world > 1 else "single GPU",
+            "l2": l2_note(p),
+            "zipf_alpha": synth.ZIPF_ALPHA if p.zipf else None}
+
+
+def l2_note(p):
+    a = 2 if p.dtype == "bf16" else 4
+    xb, wb = p.T * p.d * a, (p.E + p.S) * 3 * p.d * p.I * a
+    big = xb > L2_BYTES and wb > L2_BYTES
+    return (f"x {xb / 1e6:.0f} MB, weights {wb / 1e9:.2f} GB: " +
+            ("inputs larger than L2, no flush" if big else "weights larger than L2, no flush"
+             if wb > L2_BYTES else "smaller than L2 (parity-size workload)"))
 
 
 def run_reference(a, p):
@@ -256,7 +282,7 @@ def run_reference(a, p):
     dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
     w = synth.make_weights(p, device=dev)
     x = synth.make_x(p, w.w_router, device=dev).cpu()
-    unit = CpuOracleUnit(p, w, x, nt=256, rows=64, n_experts=1)
+    unit = CpuOracleUnit(p, w, x)
     del w
     for _ in range(a.warmup):
         unit.run()
@@ -270,8 +296,7 @@ def run_reference(a, p):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": a.gpus,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * secs / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": p.name, "T": p.T, "d": p.d, "E": p.E, "G": p.G, "K": p.K, "M": p.M, "I": p.I,
-                   "S": p.S},
+        "config": bench_config(p, a.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": CpuOracleUnit.cores(), "kind": "oracle",
                          "sample": unit.desc + " (one unit per step)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -440,6 +465,131 @@ def kernels_per_step(p):
     return n
 
 
+def load_slope(counts, top=16):
+    """Log-log slope of the sorted expert loads over the top ranks against the
+    rank of the skew direction (two experts share each of the 8 directions,
+    so ranks 2j+1 and 2j+2 both have direction rank j+1)."""
+    import numpy as np
+    c = np.sort(np.asarray(counts, np.float64))[::-1][:top]
+    r = np.arange(len(c), dtype=np.float64) // 2 + 1
+    return float(np.polyfit(np.log(r), np.log(np.maximum(c, 1.0)), 1)[0])
+
+
+def raw_routing_load(B, cfg, p, x, w_router, dev, ws):
+    """The raw load of the workload: one moe_route with bias 0 on the bench's
+    tokens, before any bias update."""
+    counts = torch.empty(p.E, dtype=torch.int32, device=dev)
+    idx = torch.empty(p.T, p.K, dtype=torch.int32, device=dev)
+    gate = torch.empty(p.T, p.K, device=dev)
+    B.moe_route(cfg, x, w_router, None, torch.zeros(p.E, device=dev), None, idx, gate, counts, ws)
+    c = counts.cpu().double()
+    return {"raw_load_max_over_mean": float(c.max() / c.mean()),
+            "raw_load_loglog_slope_top16": load_slope(c.numpy()),
+            "raw_load_note": "one routing of the bench tokens at bias 0, before warm-up; the slope is fitted "
+                             "over the 16 hottest experts against their skew-direction rank"}
+
+
+def run_cpu_baseline(p, w, x, min_seconds=10.0):
+    """The C++ oracle unit (CpuOracleUnit) run back to back for about
+    min_seconds, on the host cores, reported as the harmonic mean."""
+    unit = CpuOracleUnit(p, w, x.cpu())
+    vals, secs = [], 0.0
+    while secs < min_seconds or len(vals) < 3:
+        v, s = unit.run()
+        vals.append(v)
+        secs += s
+    return {"value": len(vals) / sum(1.0 / v for v in vals), "unit": "tokens/s", "cores": CpuOracleUnit.cores(),
+            "kind": "oracle", "sample": unit.desc + f" ({len(vals)} units)", "seconds": secs}
+
+
+def time_layer(B, cfg, p, x, weights, bias, ws, dev, steps=20, warmup=3, stage_events=False):
+    """moe_layer_forward with the workload's bias update, timed with CUDA
+    events over `steps` steps after `warmup`; optional per-stage means."""
+    out = torch.empty(p.T, p.d, dtype=synth.torch_dtype(p.dtype), device=dev)
+    idx = torch.empty(p.T, p.K, dtype=torch.int32, device=dev)
+    gate = torch.empty(p.T, p.K, dtype=torch.float32, device=dev)
+    counts = torch.empty(p.E, dtype=torch.int32, device=dev)
+
+    def step():
+        B.moe_layer_forward(cfg, x, weights, bias, p.gamma, out, idx, gate, counts, None, ws)
+
+    for _ in range(warmup):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)] if stage_events else None
+    if ev:
+        for row in ev:
+            for e in row:
+                e.record()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        if ev:
+            B.moe_set_stage_events(ev[i])
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    if ev:
+        B.moe_set_stage_events(None)
+    code = B.moe_device_error(ws)
+    if code != 0:
+        raise RuntimeError(f"device error 0x{code:x} in {p.name}")
+    ms = t0.elapsed_time(t1) / steps
+    res = {"ms_per_step": ms, "tokens_per_s": p.T / (ms * 1e-3), "steps": steps, "counts": counts.cpu()}
+    if ev:
+        res["stage_ms"] = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+                           for j, name in enumerate(STAGES)}
+    return res
+
+
+def run_other_workloads(B, w, dev, hbm, tf_sust):
+    """The decode-shape batches (T = 64 and 512) and the FP8 workload
+    (T = 32768, fp32 and power-of-two tile scales), each timed the same way
+    as the headline but for 20 steps, on the V3 weights already on the
+    device (the decode shapes share them; the FP8 workloads quantise them)."""
+    out = {}
+    wd = {k: getattr(w, k).contiguous() for k in ("w_router", "w13", "w2", "ws13", "ws2")}
+    for name in ("v3_decode_t64_bf16", "v3_decode_t512_bf16"):
+        q = synth.PRESETS[name]
+        cfg = B.config_from_preset(q)
+        ws = B.alloc_workspace(cfg, dev)
+        x = synth.make_x(q, w.w_router, device=dev)
+        bias = synth.make_bias(q, device=dev)
+        r = time_layer(B, cfg, q, x, B.make_weights(**wd), bias, ws, dev)
+        hit = int((r["counts"] > 0).sum())
+        nbytes = (hit + q.S) * 3 * q.d * q.I * 2
+        out[name] = {"ms_per_step": r["ms_per_step"], "tokens_per_s": r["tokens_per_s"], "experts_hit": hit,
+                     "weight_bytes": nbytes, "gbs": nbytes / (r["ms_per_step"] * 1e-3) / 1e9,
+                     "frac_hbm": nbytes / (r["ms_per_step"] * 1e-3) / 1e9 / hbm}
+        del ws, x
+    for name in ("v3_t32768_d7168_e256_fp8", "v3_t32768_d7168_e256_fp8_ue8m0"):
+        q = synth.PRESETS[name]
+        quant = B.moe_quantize_weights_e4m3_ue8m0 if q.expert_dtype == "e4m3_ue8m0" else B.moe_quantize_weights_e4m3
+        wq = {"w_router": wd["w_router"]}
+        for k in ("w13", "w2", "ws13", "ws2"):
+            m = wd[k]
+            qt = torch.empty(m.shape, dtype=torch.uint8, device=dev)
+            sc = torch.empty((m.shape[0], (m.shape[1] + 127) // 128, (m.shape[2] + 127) // 128),
+                             dtype=torch.float32, device=dev)
+            quant(m, qt, sc)
+            wq[k], wq[k + "_scale"] = qt, sc
+        cfg = B.config_from_preset(q)
+        ws = B.alloc_workspace(cfg, dev)
+        x = synth.make_x(q, w.w_router, device=dev)
+        bias = synth.make_bias(q, device=dev)
+        r = time_layer(B, cfg, q, x, B.make_weights(**wq), bias, ws, dev, stage_events=True)
+        g1 = flops_gemm1(q) / (r["stage_ms"]["gemm1_swiglu"] * 1e-3) / 1e12
+        out[name] = {"ms_per_step": r["ms_per_step"], "tokens_per_s": r["tokens_per_s"],
+                     "gemm1_ms": r["stage_ms"]["gemm1_swiglu"], "gemm1_tflops": g1,
+                     "gemm1_frac_fp8_sustained": g1 / (2 * tf_sust),
+                     "gemm2_routed_ms": r["stage_ms"]["gemm2_routed"]}
+        del ws, x, wq
+        torch.cuda.empty_cache()
+    out["note"] = ("same process and box as the headline, 20 timed steps after 3 warm-up steps each (forward + "
+                   "bias update); FP8 peak = 2 x the measured bf16 sustained peak (nominal fp8 / bf16 ratio)")
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(a, p):
     from mixture_experts_layer_100_b300 import binding as B
@@ -493,13 +643,13 @@ def run_ours(a, p):
             B.moe_layer_forward(cfg, xin, weights, bias, 0.0, o, idx, gate, counts, mom, ws)
             dp.global_bias_update(counts, p.T, update)
 
+    raw_load = raw_routing_load(B, cfg, p, x, wd["w_router"], dev, ws)
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
     code = B.moe_device_error(ws)
     if code != 0:
         raise RuntimeError(f"device error 0x{code:x} during warm-up")
-    raw_counts = counts.cpu()
 
     K = a.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
@@ -593,25 +743,24 @@ def run_ours(a, p):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        unit = CpuOracleUnit(p, w, x.cpu(), nt=p.T, rows=2048, n_experts=min(32, p.E))
-        v, secs = unit.run()
-        cpu = {"value": v, "unit": "tokens/s", "cores": CpuOracleUnit.cores(), "kind": "oracle",
-               "sample": unit.desc, "seconds": secs}
+        cpu = run_cpu_baseline(p, w, x)
+
+    extra = None
+    if rank == 0 and world == 1 and not a.no_extra and p.name == DEFAULT_PRESET:
+        del ws
+        torch.cuda.empty_cache()
+        extra = run_other_workloads(B, w, dev, hbm, tf_sust)
 
     clocks = sampler.summary() if rank == 0 else None
-    c = raw_counts.double()
     if rank == 0:
+        cfg_line = bench_config(p, world)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": a.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if p.expert_dtype == "bf16" else p.expert_dtype,
             "data": "synthetic (seeded; random-init weights N(0, 0.006); x ~ N(0,1) + rank-8 routing skew)",
-            "config": {"workload": p.name, "T": p.T, "d": p.d, "E": p.E, "G": p.G, "K": p.K, "M": p.M,
-                       "I": p.I, "S": p.S, "gamma": p.gamma, "global_tokens_per_step": p.T * world,
-                       "parallelism": f"dp{world} replicas" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (x 235 MB, weights 22.5 GB): no flush",
-                       "zipf_alpha": synth.ZIPF_ALPHA if p.zipf else None,
-                       "raw_load_max_over_mean": float(c.max() / c.mean())},
+            "config": cfg_line,
+            "raw_routing_load": raw_load,
             "roofline": roofline,
             "stages": stages,
             "expert_gemms": {"tflops": expert_gemm_tf, "frac_tensor_sustained": expert_gemm_tf / tf_sust,
@@ -623,6 +772,7 @@ def run_ours(a, p):
             "graph_replay": graph,
             "seq_balance": seq_balance,
             "cpu_baseline": cpu,
+            "other_workloads": extra,
             "e2e": e2e,
             "gpu_launches": kernels_per_step(p) * K,
             "clocks": clocks,

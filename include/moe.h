@@ -231,9 +231,11 @@ moe_status moe_seq_balance(const moe_config* cfg, const float* scores, const int
  *   (T = 16384, K = 8, E = 256 needs 1.5 MiB; T = 32768 needs 3 MiB).
  *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  *   library routine.
- *   The first call on each device looks up the array's device address with
- *   cudaGetSymbolAddress (with that device current) and keeps it; make that
- *   first call before any stream capture.
+ *   Every call asks cudaGetSymbolAddress for the array's address in the
+ *   current device's context, so the address always belongs to that context
+ *   (also after a device reset). The first call in a context loads the
+ *   library's device code there; make that first call before any stream
+ *   capture.
  *   All calls on a device share the one array and leave their contents in it;
  *   each call clears the part that must start at zero. Calls whose work
  *   overlaps on the GPU (other streams, other host threads) race on the array

@@ -1,8 +1,6 @@
 // moe_permute_static: the expert-major permutation of moe_permute, for
 // callers that cannot allocate device memory (see moe.h). Its scratch space
 // is one fixed array in this file instead of a caller-provided workspace.
-#include <mutex>
-
 #include "kernels.cuh"
 #include "moe.h"
 
@@ -13,25 +11,18 @@ namespace {
 // library reserves it on every GPU the process uses, until the process ends.
 static __device__ __align__(256) unsigned char g_permute_scratch[MOE_PERMUTE_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
 size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Device address of the array on the current device, looked up once per
-// device (the host-side name of the array is not a device address).
+// Device address of the array in the current context. The host-side name of
+// the array is not a device address, so it is asked for on every call: the
+// answer then always belongs to the context the call runs in (a different
+// device, a context created after a device reset). Only the first call in a
+// context loads the module there; later look-ups make no allocation and
+// queue no work.
 moe_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+  *out = p;
   return MOE_OK;
 }
 

@@ -119,3 +119,55 @@ def oracle_rows_fp8(p, w: synth.Weights, x: torch.Tensor, b: torch.Tensor, token
     return om.layer_forward_fp8_full(host(xs).astype(np.float64), host(w.w_router), W(w.w13), W(w.w2),
                                      W(w.ws13), W(w.ws2), b.cpu().numpy(), p.G, p.K, p.M, p.group_topk,
                                      ue8m0=p.expert_dtype == "e4m3_ue8m0")
+
+
+def oracle_rows_cpp(p, w: synth.Weights, x: torch.Tensor, b: torch.Tensor, tokens=None, expert_dtype=None):
+    """The C++ oracle's layer output for the given tokens (all when None),
+    streaming one expert's weights at a time to the host (so V3-sized weights
+    may stay on the device). expert_dtype: "e4m3" / "e4m3_ue8m0" for the FP8
+    path, else the master-precision path."""
+    from oracle import cpp
+    xs = host(x if tokens is None else x[torch.as_tensor(np.asarray(tokens))])
+    n = xs.shape[0]
+    s = cpp.router_scores(xs, host(w.w_router))
+    idx, gate = cpp.select_experts(s, np.asarray(b.cpu() if torch.is_tensor(b) else b, np.float32), p.G, p.K, p.M,
+                                   p.group_topk)
+    f8 = expert_dtype in ("e4m3", "e4m3_ue8m0")
+    ue = expert_dtype == "e4m3_ue8m0"
+    acc = np.zeros((n, p.d), np.float64)
+    for j in range(p.S):
+        cpp.expert_accumulate(xs, np.arange(n), host(w.ws13[j]), host(w.ws2[j]), None, acc, fp8=f8, ue8m0=ue)
+    for e in np.unique(idx):
+        rows, slots = np.nonzero(idx == e)
+        cpp.expert_accumulate(xs, rows, host(w.w13[int(e)]), host(w.w2[int(e)]), gate[rows, slots], acc, fp8=f8,
+                              ue8m0=ue)
+    return {"scores": s, "topk_idx": idx, "topk_gate": gate, "out": acc}
+
+
+def stratified_tokens(topk_idx: np.ndarray, E: int, n: int, seed: int, hot: int = 3) -> np.ndarray:
+    """A seeded token sample for the full-size parity tests that reaches every
+    expert's first and last permuted row (the first row of its first 128-row
+    tile and the last row of its ragged tail), the first and last row of every
+    tile of the `hot` most loaded experts, and uniform random tokens up to n
+    tokens in all. Positions follow the expert-major, token-ascending order of
+    the routing given (the layer's own)."""
+    from oracle import cpp
+    T, K = topk_idx.shape
+    st, _ = cpp.permutation(topk_idx, E)
+    off = cpp.exclusive_offsets(cpp.expert_counts(topk_idx, E))
+    pos = []
+    for e in range(E):
+        if off[e + 1] > off[e]:
+            pos += [off[e], off[e + 1] - 1]
+    counts = np.diff(off)
+    for e in np.argsort(-counts, kind="stable")[:hot]:
+        for p0 in range(off[e], off[e + 1], 128):
+            pos += [p0, min(p0 + 127, off[e + 1] - 1)]
+    picked = set(int(st[q]) for q in pos)
+    rng = np.random.default_rng(seed)
+    rest = rng.permutation(T)
+    for t in rest:
+        if len(picked) >= n:
+            break
+        picked.add(int(t))
+    return np.array(sorted(picked), np.int64)

@@ -7,8 +7,8 @@ import torch
 
 from mixture_experts_layer_100_b300 import synth
 from oracle import moe_oracle as om
-from tests.layer_helpers import (DEV, compare, device_weights, oracle_rows_fp8, quantize_device_weights,
-                                 run_layer)
+from tests.layer_helpers import (DEV, compare, device_weights, oracle_rows_cpp, oracle_rows_fp8,
+                                 quantize_device_weights, run_layer, stratified_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -125,10 +125,14 @@ def v3_fp8():
 
 
 def test_v3_fp8_preset_sampled_tokens(v3_fp8):
+    """The FP8 preset (T = 32768): outputs element by element against the C++
+    oracle's e4m3 path on a 1024-token sample that reaches every expert's
+    first and last permuted row and every tile of the three hottest experts."""
     p, w, wq = v3_fp8
     x = synth.make_x(p, w.w_router, device=DEV)
     b = synth.make_bias(p)
     res = run_layer(p, wq, x, b.to(DEV), gamma=p.gamma)
-    toks = np.unique(np.concatenate([np.random.default_rng(4).choice(p.T, 12, replace=False), [p.T - 1]]))
-    compare(p, res, oracle_rows_fp8(p, w, x.cpu(), b, toks), b, tokens=toks, dtype="e4m3", max_flip=0.1)
+    toks = stratified_tokens(res["topk_idx"].cpu().numpy(), p.E, 1024, seed=4)
+    compare(p, res, oracle_rows_cpp(p, w, x.cpu(), b, toks, expert_dtype="e4m3"), b, tokens=toks, dtype="e4m3",
+            max_flip=0.02)
     assert res["counts"].sum().item() == p.T * p.K

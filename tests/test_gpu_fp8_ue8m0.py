@@ -10,8 +10,8 @@ import torch
 
 from mixture_experts_layer_100_b300 import synth
 from oracle import moe_oracle as om
-from tests.layer_helpers import (DEV, compare, device_weights, oracle_rows_fp8, quantize_device_weights,
-                                 run_layer)
+from tests.layer_helpers import (DEV, compare, device_weights, oracle_rows_cpp, oracle_rows_fp8,
+                                 quantize_device_weights, run_layer, stratified_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -166,14 +166,19 @@ def test_ue8m0_entry_points_compose_to_the_layer():
 
 
 def test_v3_ue8m0_preset_sampled_tokens():
+    """The FP8 preset with power-of-two scales (T = 32768): outputs element by
+    element against the C++ oracle's UE8M0 path on a 1024-token sample that
+    reaches every expert's first and last permuted row and every tile of the
+    three hottest experts."""
     p = BASE
     w = synth.make_weights(p, device=DEV)
     wq = quantize_device_weights(device_weights(w), ue8m0=True)
     x = synth.make_x(p, w.w_router, device=DEV)
     b = synth.make_bias(p)
     res = run_layer(p, wq, x, b.to(DEV), gamma=p.gamma)
-    toks = np.unique(np.concatenate([np.random.default_rng(6).choice(p.T, 12, replace=False), [p.T - 1]]))
-    compare(p, res, oracle_rows_fp8(p, w, x.cpu(), b, toks), b, tokens=toks, dtype="e4m3_ue8m0", max_flip=0.1)
+    toks = stratified_tokens(res["topk_idx"].cpu().numpy(), p.E, 1024, seed=6)
+    compare(p, res, oracle_rows_cpp(p, w, x.cpu(), b, toks, expert_dtype="e4m3_ue8m0"), b, tokens=toks,
+            dtype="e4m3_ue8m0", max_flip=0.02)
     assert res["counts"].sum().item() == p.T * p.K
     del w, wq
     torch.cuda.empty_cache()

@@ -68,3 +68,34 @@ def test_static_scratch_permute_rejects_oversized_batch():
     p = B._ptr(dummy)
     st = B.lib.moe_permute_static(ctypes.byref(cfg), p, p, p, p, p, p, p, B._stream(None))
     assert st == 2  # MOE_ERR_UNSUPPORTED, nothing queued
+
+
+def test_static_scratch_permute_allocates_nothing():
+    """Calls after the first one leave the device's free memory and torch's
+    reserved pool exactly as they were (the scratch is the static array, not
+    a new allocation), and the Python binding of the entry point gives the
+    same bits as the C call."""
+    from mixture_experts_layer_100_b300 import binding as B
+    T, E, K, d = 4096, 64, 6, 256
+    cfg = B.make_config(T, d, E, 8, K, 3, 128, 1, 2, act="bf16")
+    idx = synth.make_topk_idx(T, E, K, seed=7).to(DEV)
+    counts = torch.from_numpy(om.expert_counts(idx.cpu().numpy(), E)).to(DEV)
+    x = torch.randn(T, d, device=DEV).to(torch.bfloat16)
+    outs = [(torch.empty(E + 1, dtype=torch.int32, device=DEV), torch.empty(T * K, dtype=torch.int32, device=DEV),
+             torch.empty(T, K, dtype=torch.int32, device=DEV), torch.empty(T * K, d, dtype=torch.bfloat16, device=DEV))
+            for _ in range(2)]
+    B.moe_permute_static(cfg, idx, counts, *outs[0][:3], x, outs[0][3])  # first call: module loaded, address looked up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    for i in range(3):
+        o = outs[i % 2]
+        B.moe_permute_static(cfg, idx, counts, *o[:3], x, o[3])
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0 and torch.cuda.memory_reserved() == reserved0
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    st, sp = om.permutation(idx.cpu().numpy(), E)
+    np.testing.assert_array_equal(outs[0][1].cpu().numpy(), st)
+    np.testing.assert_array_equal(outs[0][2].cpu().numpy(), sp)
