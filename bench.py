@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-standalone", action="store_true",
                     help="skip the standalone timing of moe_route / moe_permute")
+    ap.add_argument("--combine", choices=["gather", "scatter_add"], default=None,
+                    help="moe_layer_forward's combine mode (default: the workload's)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the decode-shape and FP8 workloads timed after the V3 bf16 headline")
     return ap.parse_args()
@@ -63,6 +65,8 @@ def parse():
 
 def preset_from_args(a):
     p = synth.PRESETS[a.preset]
+    if a.combine is not None:
+        p = p.replace(combine=a.combine)
     if a.tokens is not None:
         p = p.replace(T=a.tokens)
     if a.experts is not None:
@@ -262,7 +266,7 @@ def bench_config(p, world):
     return {"workload": p.name, "T": p.T, "d": p.d, "E": p.E, "G": p.G, "K": p.K, "M": p.M, "I": p.I, "S": p.S,
             "gamma": p.gamma, "global_tokens_per_step": p.T * world,
             "parallelism": f"dp{world} replicas" if world > 1 else "single GPU",
-            "l2": l2_note(p),
+            "l2": l2_note(p), "combine": p.combine,
             "zipf_alpha": synth.ZIPF_ALPHA if p.zipf else None}
 
 
@@ -458,6 +462,10 @@ def kernels_per_step(p):
         # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, combine, bias update
         return 10 - (1 if p.S == 0 else 0)
     n = 11  # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, routed sum, combine, bias update
+    if p.combine == "scatter_add" and p.expert_dtype == "bf16":
+        # router, select, rank, scan, scatter, shared gemm1, shared down projection (fp32 seed), gemm1,
+        # gemm2 with the scatter-add, rounding pass, bias update; S = 0: no shared GEMMs (a memset seeds)
+        return 11 if p.S > 0 else 9
     if p.S == 0:
         n -= 2  # no shared gemm1; the routed sum writes the output
     if p.expert_dtype in ("e4m3", "e4m3_ue8m0"):
@@ -540,6 +548,39 @@ def time_layer(B, cfg, p, x, weights, bias, ws, dev, steps=20, warmup=3, stage_e
         res["stage_ms"] = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
                            for j, name in enumerate(STAGES)}
     return res
+
+
+def run_combine_ab(B, p, w, x, dev, rounds=3, steps=20):
+    """Same-process A/B of the two combine modes on the headline workload:
+    `rounds` alternations of `steps` timed steps each (after 3 warm-up
+    steps), so that both see the same clock drift; the mean ms per step of
+    each mode and the routed down projection + combine stages."""
+    wd = {k: getattr(w, k).contiguous() for k in ("w_router", "w13", "w2", "ws13", "ws2")}
+    res = {}
+    for mode in ("gather", "scatter_add"):
+        q = p.replace(combine=mode)
+        cfg = B.config_from_preset(q)
+        res[mode] = {"cfg": cfg, "ws": B.alloc_workspace(cfg, dev), "ms": [], "gemm2": [], "combine": []}
+    for _ in range(rounds):
+        for mode, r in res.items():
+            q = p.replace(combine=mode)
+            bias = synth.make_bias(q, device=dev)
+            t = time_layer(B, r["cfg"], q, x, B.make_weights(**wd), bias, r["ws"], dev, steps=steps,
+                           stage_events=True)
+            r["ms"].append(t["ms_per_step"])
+            r["gemm2"].append(t["stage_ms"]["gemm2_routed"])
+            r["combine"].append(t["stage_ms"]["gemm2_shared_combine"])
+    out = {}
+    for mode, r in res.items():
+        out[mode] = {"ms_per_step": sum(r["ms"]) / rounds, "ms_per_step_each": r["ms"],
+                     "gemm2_routed_ms": sum(r["gemm2"]) / rounds, "combine_ms": sum(r["combine"]) / rounds}
+        del r["ws"]
+    torch.cuda.empty_cache()
+    out["note"] = (f"{rounds} alternating rounds of {steps} steps per mode, same process, inputs and weights; "
+                   "combine_ms is the stage after the routed down projection (gather: routed sum + shared down "
+                   "projection; scatter_add: the fp32 -> bf16 rounding pass, the shared down projection runs on "
+                   "the side stream)")
+    return out
 
 
 def run_other_workloads(B, w, dev, hbm, tf_sust):
@@ -749,7 +790,8 @@ def run_ours(a, p):
     if rank == 0 and world == 1 and not a.no_extra and p.name == DEFAULT_PRESET:
         del ws
         torch.cuda.empty_cache()
-        extra = run_other_workloads(B, w, dev, hbm, tf_sust)
+        extra = {"combine_ab": run_combine_ab(B, p, w, x, dev)}
+        extra.update(run_other_workloads(B, w, dev, hbm, tf_sust))
 
     clocks = sampler.summary() if rank == 0 else None
     if rank == 0:

@@ -72,6 +72,19 @@ typedef enum {
  *   the exponent bits of each scale are read. */
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E4M3_UE8M0 = 3 } moe_dtype;
 
+/* How moe_layer_forward combines the routed experts' rows [resmic-moe]:
+ * MOE_COMBINE_GATHER: the routed down projection writes each expert row once
+ *   (unscaled, [T*K, d] in the workspace); a per-token pass sums the K gated
+ *   rows of each token in a fixed order and the shared experts' down
+ *   projection adds that sum in its epilogue. Deterministic.
+ * MOE_COMBINE_SCATTER_ADD: the shared experts' down projection writes an fp32
+ *   [T, d] accumulator, the routed down projection's epilogue adds gate * row
+ *   into it with fp32 reductions (red.global.add), and one pass rounds it to
+ *   the output dtype. The order of the K fp32 adds per element is not fixed,
+ *   so outputs may differ in the last bits from call to call. bf16 layers
+ *   only; fp32 layers always gather. */
+typedef enum { MOE_COMBINE_GATHER = 0, MOE_COMBINE_SCATTER_ADD = 1 } moe_combine_mode;
+
 typedef struct {
   int T, d, E, G, K, M, I, S;
   int group_topk;     /* group score = sum of this many largest biased
@@ -83,6 +96,7 @@ typedef struct {
                          MOE_E4M3_UE8M0 with act MOE_BF16 (1x128 activation
                          tiles, 128x128 weight blocks, fp32 accumulation
                          [digest-3.1]) */
+  moe_combine_mode combine;  /* moe_layer_forward's combine (see above) */
 } moe_config;
 
 /* Expert weights. Element type is cfg->expert (router: cfg->act).
@@ -166,11 +180,13 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float g
                            float* bias, float* max_over_mean, moe_stream_t stream);
 
 /* The whole layer: route, permute, routed experts, shared experts with the
- * fused combine, and (when gamma != 0) the bias update, queued on `stream`.
- * The shared experts' first GEMM runs on an internal side stream (one per
- * host thread and device, created by the first call and kept until the
- * process exits) while `stream` routes and permutes; `stream` waits for it
- * before the combine, so the layer is complete when `stream` is. Make the
+ * fused combine (cfg->combine chooses how, see moe_combine_mode), and (when
+ * gamma != 0) the bias update, queued on `stream`. The shared experts' first
+ * GEMM (and, with MOE_COMBINE_SCATTER_ADD, their down projection) runs on an
+ * internal side stream (one per host thread and device, created by the first
+ * call and kept until the process exits) while `stream` routes and permutes;
+ * `stream` waits for it before the combine, so the layer is complete when
+ * `stream` is. Make the
  * first call on a device outside stream capture; later calls may be
  * captured into a CUDA graph (the side stream's fork and join become graph
  * edges, and the call makes no allocation or attribute change) and the graph
@@ -250,11 +266,11 @@ moe_status moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, co
  * on its stream at stage boundary i: 0 before the router, 1 after the router
  * GEMM, 2 after the top-K selection, 3 after the permutation, 4 after the
  * routed experts' GEMM1 (SwiGLU), 5 after the routed down projection, 6 after
- * the shared down projection with the fused combine, 7 after the bias update.
- * The shared experts' GEMM1 runs on a side stream from mark 1 on and is
- * joined before the shared down projection (between marks 5 and 6), so the
- * stages in between share the GPU with it. count must be 0 (hook off) or
- * >= 8. */
+ * the combine (gather: the routed sum and the shared down projection that
+ * adds it; scatter-add: the rounding of the accumulator), 7 after the bias
+ * update. The side stream's work starts at mark 1 and is joined between
+ * marks 5 and 6 (gather) or 4 and 5 (scatter-add), so the stages in between
+ * share the GPU with it. count must be 0 (hook off) or >= 8. */
 moe_status moe_set_stage_events(void* const* events, int count);
 
 /* Self-test of the device-side wait bound: queues one small kernel that waits

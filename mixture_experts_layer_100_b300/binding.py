@@ -29,8 +29,13 @@ class MoeError(RuntimeError):
         self.status = status
 
 
+MOE_COMBINE_GATHER, MOE_COMBINE_SCATTER_ADD = 0, 1
+_COMBINE = {"gather": MOE_COMBINE_GATHER, "scatter_add": MOE_COMBINE_SCATTER_ADD}
+
+
 class moe_config(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("T", "d", "E", "G", "K", "M", "I", "S", "group_topk", "act", "expert")]
+    _fields_ = [(n, ctypes.c_int) for n in ("T", "d", "E", "G", "K", "M", "I", "S", "group_topk", "act", "expert",
+                                            "combine")]
 
 
 class moe_weights(ctypes.Structure):
@@ -93,13 +98,13 @@ def _check(fn: str, status: int):
         raise MoeError(fn, status)
 
 
-def make_config(T, d, E, G, K, M, I, S, group_topk=2, act="bf16", expert=None) -> moe_config:
-    return moe_config(T, d, E, G, K, M, I, S, group_topk, _DT[act], _DT[expert or act])
+def make_config(T, d, E, G, K, M, I, S, group_topk=2, act="bf16", expert=None, combine="gather") -> moe_config:
+    return moe_config(T, d, E, G, K, M, I, S, group_topk, _DT[act], _DT[expert or act], _COMBINE[combine])
 
 
-def config_from_preset(p, T: Optional[int] = None) -> moe_config:
+def config_from_preset(p, T: Optional[int] = None, combine: Optional[str] = None) -> moe_config:
     return make_config(p.T if T is None else T, p.d, p.E, p.G, p.K, p.M, p.I, p.S, p.group_topk,
-                       p.dtype, p.expert_dtype)
+                       p.dtype, p.expert_dtype, combine or p.combine)
 
 
 def make_weights(w_router=None, w13=None, w2=None, ws13=None, ws2=None, w13_scale=None, w2_scale=None,

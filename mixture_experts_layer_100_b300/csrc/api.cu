@@ -23,12 +23,13 @@ moe_status check_config(const moe_config* c) {
   if (c->act != MOE_F32 && c->act != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->expert != c->act && !(is_f8(c->expert) && c->act == MOE_BF16)) return MOE_ERR_INVALID_ARG;
   if ((long long)c->T * c->K > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (c->combine != MOE_COMBINE_GATHER && c->combine != MOE_COMBINE_SCATTER_ADD) return MOE_ERR_INVALID_ARG;
   if (c->act == MOE_BF16) {
     if (c->d % 128 != 0 || c->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->E > 256) return MOE_ERR_UNSUPPORTED;
     if (is_f8(c->expert) && c->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
-  } else if (c->d % 4 != 0) {
-    return MOE_ERR_UNSUPPORTED;
+  } else if (c->d % 128 != 0 || c->I % 128 != 0) {
+    return MOE_ERR_UNSUPPORTED;  // fp32 layers run the same tcgen05 tiles (as tf32 pairs)
   }
   return MOE_OK;
 }
@@ -136,6 +137,13 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const float* x
   if (!ok_ptr(xp) || !ok_ptr(offsets) || !ok_ptr(yp)) return MOE_ERR_INVALID_ARG;
   if (is_f8(c.expert) && !ok_ptr(xp_scale)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (c.act == MOE_F32) {
+    // the caller's fp32 rows and the expert weights as tf32 pairs
+    void* xps = at<void>(ws, layout(c).xp);
+    MOE_TRY(split_rows_f32(xp, (long long)c.T * c.K, c.d, xps, st));
+    MOE_TRY(split_weights_f32(c, w, false, true, false, ws, st));
+    xp = xps;
+  }
   MOE_TRY(gemm1_stage(c, xp, xp_scale, offsets, nullptr, w, true, false, ws, st));
   MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
   return MOE_OK;
@@ -152,6 +160,12 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
   if (c.S > 0 && !ok_ptr(x)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (c.S > 0) {
+    if (c.act == MOE_F32) {
+      void* xs = at<void>(ws, layout(c).xs);
+      MOE_TRY(split_rows_f32(x, c.T, c.d, xs, st));
+      MOE_TRY(split_weights_f32(c, w, false, false, true, ws, st));
+      x = xs;
+    }
     if (is_f8(c.expert)) {
       const Layout Lw = layout(c);
       MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
@@ -191,22 +205,38 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
   if (c.T > 0) {
     float* scores = at<float>(ws, Lw.scores);
     const bool f8 = is_f8(c.expert);
-    MOE_TRY(router_scores(c, x, w->w_router, scores, ws, st));
+    const bool f32 = c.act == MOE_F32;
+    const void* w_router = w->w_router;
+    if (f32) {
+      // fp32 layer: x and every weight as tf32 pairs for the tensor cores
+      void* xs = at<void>(ws, Lw.xs);
+      MOE_TRY(split_rows_f32(x, c.T, c.d, xs, st));
+      MOE_TRY(split_weights_f32(c, w, true, true, true, ws, st));
+      x = xs;
+      w_router = f32_weights(c, ws).wr;
+    }
+    MOE_TRY(router_scores(c, x, w_router, scores, ws, st));
     MOE_TRY(stage_mark(1, st));
     // The shared experts' GEMM1 depends on x only: it runs on a side stream,
     // overlapping the memory-bound selection and permutation below; the main
-    // stream waits for it before the shared down projection.
+    // stream waits for it before the shared down projection. With the
+    // scatter-add combine the side stream also runs the shared down
+    // projection, which writes the fp32 accumulator (zeros when S = 0), and
+    // the main stream waits before the routed down projection adds into it.
+    const bool scat = scatter_combine(c);
+    float* acc = f32 ? static_cast<float*>(out) : at<float>(ws, Lw.acc);  // fp32 layers add into out itself
     SideStream* side = nullptr;
-    if (c.S > 0) {
+    if (c.S > 0 || scat) {
       MOE_TRY(side_stream(&side));
       MOE_CUDA(cudaEventRecord(side->fork, st));
       MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-      if (f8) {
+      if (f8 && c.S > 0) {
         MOE_CUDA(launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), c.T, c.d, at<uint8_t>(ws, Lw.xq),
                                       at<float>(ws, Lw.xq_scale), c.expert == MOE_E4M3_UE8M0, num_sms(),
                                       side->s));
       }
-      MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, side->s));
+      if (c.S > 0) MOE_TRY(gemm1_stage(c, nullptr, nullptr, nullptr, x, w, false, true, ws, side->s));
+      if (scat) MOE_TRY(shared_seed_stage(c, w, acc, ws, side->s));
       MOE_CUDA(cudaEventRecord(side->join, side->s));
     }
     MOE_CUDA(launch_route_select(scores, bias, c.T, c.E, c.G, c.K, c.M, c.group_topk, topk_idx, topk_gate, counts,
@@ -217,14 +247,22 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
     void* xp = at<void>(ws, Lw.xp);
     void* yp = at<void>(ws, Lw.yp);
     MOE_TRY(permute_stage(c, topk_idx, counts, offsets, at<int32_t>(ws, Lw.sorted_tok), slot_pos, x, xp,
-                          f8 ? at<float>(ws, Lw.xp_scale) : nullptr, nullptr, nullptr, ws, st));
+                          f8 ? at<float>(ws, Lw.xp_scale) : nullptr, nullptr, nullptr, ws, st,
+                          scat ? topk_gate : nullptr, scat ? at<float>(ws, Lw.gate_p) : nullptr, f32));
     MOE_TRY(stage_mark(3, st));
     MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, false, ws, st));
     MOE_TRY(stage_mark(4, st));
-    MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
-    MOE_TRY(stage_mark(5, st));
-    if (side != nullptr) MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
-    MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));
+    if (scat) {
+      MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+      MOE_TRY(gemm2_scatter_stage(c, offsets, w, acc, ws, st));
+      MOE_TRY(stage_mark(5, st));
+      if (!f32) MOE_TRY(acc_round_stage(c, acc, out, st));
+    } else {
+      MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
+      MOE_TRY(stage_mark(5, st));
+      if (side != nullptr) MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+      MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));
+    }
     MOE_TRY(stage_mark(6, st));
     if (gamma != 0.0f)
       MOE_CUDA(launch_bias_update(counts, c.E, (long long)c.T * c.K, gamma, bias, max_over_mean, st));

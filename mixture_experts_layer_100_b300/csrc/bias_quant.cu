@@ -114,7 +114,32 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
   }
 }
 
+// Rows of fp32 values split for the three-product tf32 GEMMs: row r of src
+// [rows, cols] becomes dst[r] = [hi (cols) | lo (cols)], hi = tf32_hi(x),
+// lo = x - hi. Four values per thread and iteration.
+__global__ void __launch_bounds__(256) split_tf32_kernel(const float4* __restrict__ src, long long rows, int cols4,
+                                                         float4* __restrict__ dst) {
+  const long long n = rows * cols4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / cols4;
+    const int c = (int)(i - r * cols4);
+    const float4 v = src[i];
+    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+    dst[2 * r * cols4 + c] = h;
+    dst[2 * r * cols4 + cols4 + c] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_split_tf32(const float* src, long long rows, int cols, float* dst, int num_sms, cudaStream_t st) {
+  const long long n = rows * (cols / 4);
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)std::max(1LL, std::min((n + 255) / 256, (long long)num_sms * 8));
+  split_tf32_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src), rows, cols / 4,
+                                            reinterpret_cast<float4*>(dst));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bias_update(const int* counts, int E, long long TK, float gamma, float* bias,
                                float* max_over_mean, cudaStream_t st) {

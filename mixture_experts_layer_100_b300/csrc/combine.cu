@@ -1,119 +1,10 @@
-// fp32 expert GEMMs on the CUDA cores (FFMA), for layers whose activations
-// and weights are fp32: the output tolerance of such a layer (1e-5 of the
-// largest output) is below what TF32 tensor-core inputs can deliver, so these
-// shapes stay on plain fp32 arithmetic. 64 x 64 output tiles, K staged through
-// shared memory in steps of 16, 4 x 4 outputs per thread.
+// The combine's memory-bound passes: the per-token gate-weighted sum of the
+// routed rows (gather form) and the rounding of the fp32 accumulator (scatter
+// form).
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int kT = 64;
-constexpr int kK = 16;
-
-__device__ __forceinline__ float load_b(const SimtParams& p, int g, int n, int k, int up) {
-  if (p.mode == kSimtSwiGLU) {
-    // out column n of the gate (up = 0) or up (up = 1) projection
-    int e = g, nn = n;
-    if (p.shared) {
-      e = n / p.I;
-      nn = n % p.I;
-    }
-    return p.B[((size_t)e * 2 * p.I + (size_t)up * p.I + nn) * p.Kdim + k];
-  }
-  int e = g, kk = k;
-  if (p.shared) {
-    e = k / p.I;
-    kk = k % p.I;
-  }
-  return p.B[((size_t)e * p.N + n) * p.I + kk];
-}
-
-__global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
-  __shared__ float As[kT][kK + 1];
-  __shared__ float Bg[kT][kK + 1];
-  __shared__ float Bu[kT][kK + 1];
-  __shared__ int s_info[3];  // group, row0, row_end
-  if (threadIdx.x == 0) {
-    int mi = blockIdx.y, g = -1, row0 = 0, row_end = 0;
-    if (p.groups > 0) {
-      for (int e = 0; e < p.groups; ++e) {
-        const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
-        const int mt = (o1 - o0 + kT - 1) / kT;
-        if (mi < mt) {
-          g = e;
-          row0 = o0 + mi * kT;
-          row_end = o1;
-          break;
-        }
-        mi -= mt;
-      }
-    } else if (mi * kT < p.rows) {
-      g = 0;
-      row0 = mi * kT;
-      row_end = p.rows;
-    }
-    s_info[0] = g;
-    s_info[1] = row0;
-    s_info[2] = row_end;
-  }
-  __syncthreads();
-  const int g = s_info[0], row0 = s_info[1], row_end = s_info[2];
-  if (g < 0) return;
-  const int n0 = blockIdx.x * kT;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads, 4 x 4 each
-  const bool swiglu = p.mode == kSimtSwiGLU;
-  float ag[4][4] = {}, au[4][4] = {};
-  for (int k0 = 0; k0 < p.Kdim; k0 += kK) {
-    for (int i = threadIdx.x; i < kT * kK; i += 256) {
-      const int r = i / kK, c = i % kK;
-      const int row = row0 + r, k = k0 + c, n = n0 + r;
-      As[r][c] = (row < row_end && k < p.Kdim) ? p.A[(size_t)row * p.lda + k] : 0.0f;
-      const bool okb = n < p.N && k < p.Kdim;
-      Bg[r][c] = okb ? load_b(p, g, n, k, 0) : 0.0f;
-      if (swiglu) Bu[r][c] = okb ? load_b(p, g, n, k, 1) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kK; ++k) {
-      float a[4], bg[4], bu[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = As[ty * 4 + i][k];
-        bg[i] = Bg[tx * 4 + i][k];
-        bu[i] = swiglu ? Bu[tx * 4 + i][k] : 0.0f;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ag[i][j] = fmaf(a[i], bg[j], ag[i][j]);
-          au[i][j] = fmaf(a[i], bu[j], au[i][j]);
-        }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int row = row0 + ty * 4 + i;
-    if (row >= row_end) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n >= p.N) continue;
-      float v = ag[i][j];
-      if (swiglu) {
-        v = silu(v) * au[i][j];
-      } else if (p.mode == kSimtCombine) {
-        for (int k = 0; k < p.topk; ++k) {
-          const int pos = p.slot_pos[(size_t)row * p.topk + k];
-          v = fmaf(p.gate[(size_t)row * p.topk + k], p.yp[(size_t)pos * p.N + n], v);
-        }
-      }
-      p.out[(size_t)row * p.ldo + n] = v;
-    }
-  }
-}
 
 // out[t] = sum_k gate[t,k] * yp[slot_pos[t,k]] when there are no shared experts.
 template <typename Tv>
@@ -189,7 +80,32 @@ __global__ void __launch_bounds__(256) routed_sum_bf16_kernel(const uint4* __res
   }
 }
 
+// out = bf16(acc), 8 values per thread and iteration (two 16-byte loads, one
+// 16-byte store).
+__global__ void __launch_bounds__(256) acc_to_bf16_kernel(const float4* __restrict__ acc, size_t n8,
+                                                          uint4* __restrict__ out) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = __ldcs(acc + 2 * i), b = __ldcs(acc + 2 * i + 1);
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+    uint4 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&h0);
+    o.y = *reinterpret_cast<const uint32_t*>(&h1);
+    o.z = *reinterpret_cast<const uint32_t*>(&h2);
+    o.w = *reinterpret_cast<const uint32_t*>(&h3);
+    out[i] = o;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_acc_to_bf16(const float* acc, size_t n, void* out, int num_sms, cudaStream_t st) {
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n8 + 255) / 256, (size_t)num_sms * 8));
+  acc_to_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc), n8, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_routed_sum_bf16(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
                                    void* r, int num_sms, cudaStream_t st) {
@@ -205,15 +121,6 @@ cudaError_t launch_routed_sum_bf16(const void* yp, const int* slot_pos, const fl
   }
   return cudaGetLastError();
 }
-
-cudaError_t launch_simt_gemm(const SimtParams& p, int max_mtiles, cudaStream_t st) {
-  if (max_mtiles <= 0) return cudaSuccess;
-  dim3 grid((p.N + kT - 1) / kT, max_mtiles);
-  simt_gemm_kernel<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
-int simt_max_mtiles(int rows_total, int groups) { return (rows_total + kT - 1) / kT + groups; }
 
 cudaError_t launch_gather_combine(const void* yp, const int* slot_pos, const float* gate, int T, int d, int topk,
                                   bool bf16, void* out, int num_sms, cudaStream_t st) {

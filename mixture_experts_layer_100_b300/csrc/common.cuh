@@ -73,6 +73,23 @@ inline cudaError_t set_smem_once(F kern, int bytes, int (&done)[64]) {
   return e;
 }
 
+// Selection key of a biased affinity v of expert e: the order-preserving bits
+// of v above the complement of e, so that the larger key is the larger value
+// and, among equal values, the lower expert index. -0 and +0 share a key.
+__device__ __forceinline__ uint64_t score_key(float v, int e) {
+  if (v == 0.0f) v = 0.0f;
+  uint32_t b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)b << 32) | (uint32_t)(~(uint32_t)e);
+}
+
+// High part of x for the three-product tf32 GEMMs: x rounded to the nearest
+// value with 10 mantissa bits (which tf32 holds exactly; ties away from
+// zero). x - tf32_hi(x) is exact in fp32 and at most 2^-11 |x|.
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
 // e4m3 code of v (round to nearest even, saturating to +/-448).
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
   return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);

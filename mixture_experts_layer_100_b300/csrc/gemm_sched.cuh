@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -27,12 +28,14 @@ struct Sched {
   const int* off;   // [groups0 + 1] row offsets
   int groups0, tiles0, total;
   int n_tiles0, n_tiles1, mt1, rows1;
+  int bm = kBM;                // rows per tile
+  int super_row = kSuperRow;   // m-tiles walked together per n sweep
 
-  __device__ __forceinline__ static void raster(int local, int mt, int nt, int& m, int& n) {
-    const int sr = local / (kSuperRow * nt);
-    const int base = sr * kSuperRow;
-    const int h = min(kSuperRow, mt - base);
-    const int rem = local - sr * kSuperRow * nt;
+  __device__ __forceinline__ void raster(int local, int mt, int nt, int& m, int& n) const {
+    const int sr = local / (super_row * nt);
+    const int base = sr * super_row;
+    const int h = min(super_row, mt - base);
+    const int rem = local - sr * super_row * nt;
     n = rem / h;
     m = base + rem % h;
   }
@@ -48,13 +51,13 @@ struct Sched {
       t.seg = 0;
       t.group = lo;
       raster(L - tp[lo], mt[lo], n_tiles0, t.m, t.n);
-      t.row0 = off[lo] + t.m * kBM;
+      t.row0 = off[lo] + t.m * bm;
       t.row_end = off[lo + 1];
     } else {
       t.seg = 1;
       t.group = 0;
       raster(L - tiles0, mt1, n_tiles1, t.m, t.n);
-      t.row0 = t.m * kBM;
+      t.row0 = t.m * bm;
       t.row_end = rows1;
     }
     return t;
@@ -98,6 +101,29 @@ __device__ __forceinline__ void warp_store_rows64(uint8_t* stg, int lane, const 
     const int r = 8 * k + (lane >> 2), j = lane & 3;
     const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
     if (r < nrows) *reinterpret_cast<uint4*>(base + (size_t)r * pitch + 16 * j) = v;
+  }
+  __syncwarp();
+}
+
+// The reduction form of warp_store_rows64 for fp32 rows: lane r holds 16 fp32
+// values of row r in w[0..3]; they are added (red.global.add, 16 bytes at a
+// time) to dst + tok(r) * pitch, where tok(r) is the `tok` value of lane r.
+// The same staging block and layout make each instruction cover 8 rows x 64
+// contiguous bytes. Rows r >= nrows are skipped. Every lane of the warp must
+// call it.
+__device__ __forceinline__ void warp_red_rows64(uint8_t* stg, int lane, const uint4 (&w)[4], float* dst, int tok,
+                                                size_t pitch, int nrows) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = w[j];
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2), j = lane & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+    const int tr = __shfl_sync(0xffffffffu, tok, r);
+    if (r < nrows)
+      ptx::red_add_v4_f32(dst + (size_t)tr * pitch + 4 * j, __uint_as_float(v.x), __uint_as_float(v.y),
+                          __uint_as_float(v.z), __uint_as_float(v.w));
   }
   __syncwarp();
 }

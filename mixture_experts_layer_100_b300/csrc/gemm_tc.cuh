@@ -1,5 +1,6 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for
-// sm_103a, bf16 operands, fp32 accumulation in tensor memory.
+// sm_103a, bf16 operands (or fp32 operands as tf32 pairs), fp32 accumulation
+// in tensor memory.
 //
 // C[row, n] = sum_k A[row, k] * B_g[n, k] for every row of group g. Both
 // operands are K-major and are moved global -> shared by TMA with 128-byte
@@ -31,6 +32,8 @@ enum class Epi : int {
   kSwiGLU = 1,         // out bf16 [rows, ldo] = silu(gate) * up  (128 cols per tile)
   kStore = 2,          // out bf16 [rows, ldo] = acc
   kCombine = 3,        // out bf16 [T, ldo] = acc + radd (the gate-weighted routed sum)
+  kStoreF32 = 4,       // out fp32 [rows, ldo] = acc
+  kScatterAdd = 5,     // out fp32 [T, ldo]: out[sorted_tok[row]] += gate_p[row] * acc (reductions)
 };
 
 struct TcGemmParams {
@@ -47,12 +50,21 @@ struct TcGemmParams {
   // kCombine: per-token routed sum r[t] = sum_k gate[t,k] * yp[slot_pos[t,k]],
   // [T, ldo1] bf16, added to the shared experts' output in the epilogue
   const __nv_bfloat16* radd;
+  const float* radd_f32;  // kCombine with fp32 (tf32-pair) operands: fp32 [T, ldo1]
+  // kScatterAdd: token of each permuted row and its gate (segment 0 rows)
+  const int* sorted_tok;
+  const float* gate_p;
   int* err;             // device error word
 };
 
 struct TcGemmLaunch {
   Epi epi;
   int bn;
+  int mh = 1;  // 128-row halves per tile (expert GEMMs: 1 or 2)
+  // fp32 operands as tf32 pairs: every operand row holds its tf32 high part
+  // and its remainder ([.., 2, K]); the product is taken as hi*hi + hi*lo +
+  // lo*hi with kind::tf32 MMAs
+  bool split = false;
   CUtensorMap a0, b0, a1, b1;
   TcGemmParams p;
   int grid;

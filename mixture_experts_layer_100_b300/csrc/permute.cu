@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     permute_scatter_kernel(const int* __restrict__ topk_idx, const int* __restrict__ local_rank,
                            const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
                            const VecT* __restrict__ x, int row_vecs, int* __restrict__ sorted_tok,
-                           int* __restrict__ slot_pos, VecT* __restrict__ xp) {
+                           int* __restrict__ slot_pos, VecT* __restrict__ xp, const float* __restrict__ gate_in,
+                           float* __restrict__ gate_p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     int pos = 0;
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         pos = chunk_base[(size_t)e * nchunks + t / kChunk] + local_rank[(size_t)t * K + lane];
         slot_pos[(size_t)t * K + lane] = pos;
         sorted_tok[pos] = t;
+        if (gate_p != nullptr) gate_p[pos] = gate_in[(size_t)t * K + lane];
       } else {
         pos = -1;
       }
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                                 const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
                                 const __nv_bfloat16* __restrict__ x, int d, int* __restrict__ sorted_tok,
                                 int* __restrict__ slot_pos, uint8_t* __restrict__ xp, float* __restrict__ tok_scale,
-                                uint8_t* __restrict__ xq, bool ue8m0) {
+                                uint8_t* __restrict__ xq, bool ue8m0, const float* __restrict__ gate_in,
+                                float* __restrict__ gate_p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = d / 128;
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
@@ -168,6 +171,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         pos = chunk_base[(size_t)e * nchunks + t / kChunk] + local_rank[(size_t)t * K + lane];
         slot_pos[(size_t)t * K + lane] = pos;
         sorted_tok[pos] = t;
+        if (gate_p != nullptr) gate_p[pos] = gate_in[(size_t)t * K + lane];
       }
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
@@ -279,17 +283,17 @@ cudaError_t launch_permute_scan(const int* counts, const int* chunk_hist, int T,
 
 cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, const int* chunk_base, int T, int K,
                                    int E, const void* x, size_t row_bytes, int* sorted_tok, int* slot_pos, void* xp,
-                                   int num_sms, cudaStream_t st) {
+                                   int num_sms, cudaStream_t st, const float* gate_in, float* gate_p) {
   const int nchunks = permute_chunks(T);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
   if (row_bytes % 16 == 0) {
     permute_scatter_kernel<uint4><<<blocks, kWarps * 32, 0, st>>>(
         topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint4*>(x), (int)(row_bytes / 16),
-        sorted_tok, slot_pos, static_cast<uint4*>(xp));
+        sorted_tok, slot_pos, static_cast<uint4*>(xp), gate_in, gate_p);
   } else {
     permute_scatter_kernel<uint32_t><<<blocks, kWarps * 32, 0, st>>>(
         topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint32_t*>(x), (int)(row_bytes / 4),
-        sorted_tok, slot_pos, static_cast<uint32_t*>(xp));
+        sorted_tok, slot_pos, static_cast<uint32_t*>(xp), gate_in, gate_p);
   }
   return cudaGetLastError();
 }
@@ -297,11 +301,13 @@ cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, c
 cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
                                         int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
                                         uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, float* tok_scale,
-                                        bool ue8m0, int num_sms, cudaStream_t st) {
+                                        bool ue8m0, int num_sms, cudaStream_t st, const float* gate_in,
+                                        float* gate_p) {
   const int nchunks = permute_chunks(T);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
   permute_scatter_e4m3_kernel<<<blocks, kWarps * 32, 0, st>>>(topk_idx, local_rank, chunk_base, T, K, E, nchunks, x,
-                                                              d, sorted_tok, slot_pos, xp, tok_scale, xq, ue8m0);
+                                                              d, sorted_tok, slot_pos, xp, tok_scale, xq, ue8m0,
+                                                              gate_in, gate_p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int ntiles = d / 128;

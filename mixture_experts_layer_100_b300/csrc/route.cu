@@ -13,13 +13,6 @@ namespace {
 
 constexpr int kWarps = 8;
 
-__device__ __forceinline__ uint64_t score_key(float v, int e) {
-  if (v == 0.0f) v = 0.0f;  // -0 and +0 compare equal: give them one key
-  uint32_t b = __float_as_uint(v);
-  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return ((uint64_t)b << 32) | (uint32_t)(~(uint32_t)e);
-}
-
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -158,43 +151,6 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// Router for fp32 activations: s = sigmoid(x W_r^T), plain FMA tiles
-// (64 tokens x 32 experts per block, K staged through shared memory).
-__global__ void __launch_bounds__(256) router_f32_kernel(const float* __restrict__ x, const float* __restrict__ wr,
-                                                         int T, int d, int E, float* __restrict__ scores) {
-  __shared__ float xs[64][33];
-  __shared__ float ws[32][33];
-  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int k0 = 0; k0 < d; k0 += 32) {
-    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-      const int r = i / 32, c = i % 32;
-      xs[r][c] = (t0 + r < T && k0 + c < d) ? x[(size_t)(t0 + r) * d + k0 + c] : 0.0f;
-    }
-    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
-      const int r = i / 32, c = i % 32;
-      ws[r][c] = (e0 + r < E && k0 + c < d) ? wr[(size_t)(e0 + r) * d + k0 + c] : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float w = ws[tx][k];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(xs[ty + 8 * i][k], w, acc[i]);
-    }
-    __syncthreads();
-  }
-  const int e = e0 + tx;
-  if (e < E) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = t0 + ty + 8 * i;
-      if (t < T) scores[(size_t)t * E + e] = 1.0f / (1.0f + expf(-acc[i]));
-    }
-  }
-}
-
 // Sequence-wise balance statistic of the routing (the DeepSeek-V3 report's
 // sequence-level balance loss, which the digest's section 2.2 keeps with a
 // tiny weight), one block per run of seq_len tokens:
@@ -305,12 +261,6 @@ cudaError_t launch_route_select(const float* scores, const float* bias, int T, i
       }
   }
 #undef MOE_ROUTE_CASE
-  return cudaGetLastError();
-}
-
-cudaError_t launch_router_f32(const float* x, const float* wr, int T, int d, int E, float* scores, cudaStream_t st) {
-  dim3 grid((T + 63) / 64, (E + 31) / 32);
-  router_f32_kernel<<<grid, 256, 0, st>>>(x, wr, T, d, E, scores);
   return cudaGetLastError();
 }
 

@@ -2,6 +2,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "gemm_fp8.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
@@ -31,16 +33,27 @@ Layout layout(const moe_config& c) {
   L.offsets = take((E + 1) * 4);
   L.sorted_tok = take(TK * 4);
   L.slot_pos = take(TK * 4);
-  L.xp = take(TK * d * ex);
+  const size_t pairs = c.act == MOE_F32 ? 2 : 1;  // fp32 GEMM operands are stored as tf32 pairs
+  L.xp = take(TK * d * ex * pairs);
   L.xp_scale = take(f8 ? (d / 128) * TK * 4 : 0);
   L.xq = take(f8 ? T * d : 0);
   L.xq_scale = take(f8 ? (d / 128) * T * 4 : 0);
   L.tok_scale = take(f8 ? (d / 128) * T * 4 : 0);
-  L.h = take(TK * I * ex);
+  L.h = take(TK * I * ex * pairs);
   L.h_scale = take(f8 ? (I / 128) * TK * 4 : 0);
-  L.hs = take(T * S * I * ex);
+  L.hs = take(T * S * I * ex * pairs);
   L.hs_scale = take(f8 ? (S * I / 128) * T * 4 : 0);
-  L.yp = take(TK * d * ea);
+  const bool scat = scatter_combine(c);
+  L.yp = take(scat ? 0 : TK * d * ea);
+  L.gate_p = take(scat ? TK * 4 : 0);
+  L.acc = take(scat && c.act == MOE_BF16 ? T * d * 4 : 0);  // fp32 layers add into out itself
+  const bool f32 = c.act == MOE_F32;
+  L.xs = take(f32 ? T * 2 * d * 4 : 0);
+  L.wr_s = take(f32 ? E * 2 * d * 4 : 0);
+  L.w13_s = take(f32 ? E * 2 * I * 2 * d * 4 : 0);
+  L.w2_s = take(f32 ? E * d * 2 * I * 4 : 0);
+  L.ws13_s = take(f32 ? S * 2 * I * 2 * d * 4 : 0);
+  L.ws2_s = take(f32 ? S * d * 2 * I * 4 : 0);
   L.total = o;
   return L;
 }
@@ -102,7 +115,45 @@ static moe_status map_3d(CUtensorMap* m, const void* ptr, size_t elem, uint64_t 
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+// fp32 tf32 pairs: [n_mat,] rows, 2, K (K innermost), box [1,] box_rows, 1, 32
+// (one 128-byte swizzle row of 32 fp32 per row and part). n_mat = 0: 3-D.
+static moe_status map_pairs(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint64_t n_mat,
+                            uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MOE_ERR_CUDA;
+  const int rank = n_mat ? 4 : 3;
+  cuuint64_t dims[4] = {K, 2, rows, n_mat ? n_mat : 1};
+  cuuint64_t strides[3] = {K * 4, 2 * K * 4, rows * 2 * K * 4};
+  cuuint32_t box[4] = {32, 1, box_rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 static int down_bn(int d) { return d % 256 == 0 ? 256 : 128; }
+
+// 128-row halves per tile of the bf16 routed experts' GEMM1: 2 (256-row tiles
+// whose halves share each staged weight slice, a third less operand traffic
+// from L2) when the experts average at least two full 128-row tiles, else 1
+// (256-row tiles stage fewer K slices, which starves the weight-streaming
+// decode shapes). The other expert GEMMs measured faster with 1.
+// MOE_GEMM_TILE_ROWS=128 or 256 forces one size for every expert GEMM (read
+// once per process; a switch for comparisons, results are identical).
+static int forced_tile_halves() {
+  static int mh = -1;
+  if (mh < 0) {
+    const char* v = getenv("MOE_GEMM_TILE_ROWS");
+    mh = v == nullptr ? 0 : atoi(v) == 128 ? 1 : atoi(v) == 256 ? 2 : 0;
+  }
+  return mh;
+}
+
+static int expert_tile_halves(const moe_config& c, bool routed_gemm1) {
+  if (forced_tile_halves() != 0) return forced_tile_halves();
+  return routed_gemm1 && (long long)c.T * c.K >= 256LL * c.E ? 2 : 1;
+}
 
 static int router_bn(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
 
@@ -111,30 +162,65 @@ static int tc_grid(long long tiles_upper) {
 }
 
 // ------------------------------------------------------------ stages
-moe_status router_scores(const moe_config& c, const void* x, const void* w_router, float* s, void* ws,
-                         cudaStream_t st) {
-  if (c.act == MOE_F32) {
-    MOE_CUDA(launch_router_f32(static_cast<const float*>(x), static_cast<const float*>(w_router), c.T, c.d, c.E, s,
-                               st));
-    return MOE_OK;
-  }
+// The router GEMM with the sigmoid in its epilogue.
+static moe_status router_gemm(const moe_config& c, const void* x, const void* w_router, float* s, void* ws,
+                              cudaStream_t st) {
   TcGemmLaunch L{};
   L.epi = Epi::kRouterSigmoid;
   L.bn = router_bn(c.E);
-  MOE_TRY(map_2d(&L.a1, x, 2, c.d, c.T, 64, 128));
-  MOE_TRY(map_2d(&L.b1, w_router, 2, c.d, c.E, 64, L.bn));
+  if (c.act == MOE_F32) {
+    // x and w_router as tf32 pairs
+    L.split = true;
+    MOE_TRY(map_pairs(&L.a1, x, c.d, c.T, 0, 128));
+    MOE_TRY(map_pairs(&L.b1, w_router, c.d, c.E, 0, L.bn));
+    L.p.k_blocks1 = c.d / 32;
+  } else {
+    MOE_TRY(map_2d(&L.a1, x, 2, c.d, c.T, 64, 128));
+    MOE_TRY(map_2d(&L.b1, w_router, 2, c.d, c.E, 64, L.bn));
+    L.p.k_blocks1 = c.d / 64;
+  }
   L.a0 = L.a1;
   L.b0 = L.b1;
   L.p.groups0 = 0;
   L.p.rows1 = c.T;
-  L.p.n_tiles1 = 1;
-  L.p.k_blocks1 = c.d / 64;
+  L.p.n_tiles1 = (c.E + L.bn - 1) / L.bn;  // more than one only past 256 experts (fp32 layers)
   L.p.out1 = s;
   L.p.n_valid = c.E;
   L.p.err = at<int>(ws, 0);
-  L.grid = tc_grid((c.T + 127) / 128);
+  L.grid = tc_grid((long long)((c.T + 127) / 128) * L.p.n_tiles1);
   L.stream = st;
   MOE_CUDA(launch_tc_gemm(L));
+  return MOE_OK;
+}
+
+moe_status router_scores(const moe_config& c, const void* x, const void* w_router, float* s, void* ws,
+                         cudaStream_t st) {
+  return router_gemm(c, x, w_router, s, ws, st);
+}
+
+F32W f32_weights(const moe_config& c, void* ws) {
+  const Layout L = layout(c);
+  return F32W{at<float>(ws, L.wr_s), at<float>(ws, L.w13_s), at<float>(ws, L.w2_s), at<float>(ws, L.ws13_s),
+              at<float>(ws, L.ws2_s)};
+}
+
+moe_status split_rows_f32(const void* src, long long rows, int cols, void* dst, cudaStream_t st) {
+  MOE_CUDA(launch_split_tf32(static_cast<const float*>(src), rows, cols, static_cast<float*>(dst), num_sms(), st));
+  return MOE_OK;
+}
+
+moe_status split_weights_f32(const moe_config& c, const moe_weights* w, bool router, bool routed, bool shared,
+                             void* ws, cudaStream_t st) {
+  const F32W f = f32_weights(c, ws);
+  if (router) MOE_TRY(split_rows_f32(w->w_router, c.E, c.d, f.wr, st));
+  if (routed) {
+    MOE_TRY(split_rows_f32(w->w13, (long long)c.E * 2 * c.I, c.d, f.w13, st));
+    MOE_TRY(split_rows_f32(w->w2, (long long)c.E * c.d, c.I, f.w2, st));
+  }
+  if (shared && c.S > 0) {
+    MOE_TRY(split_rows_f32(w->ws13, (long long)c.S * 2 * c.I, c.d, f.ws13, st));
+    MOE_TRY(split_rows_f32(w->ws2, (long long)c.S * c.d, c.I, f.ws2, st));
+  }
   return MOE_OK;
 }
 
@@ -146,6 +232,14 @@ moe_status route_stage(const moe_config& c, const void* x, const void* w_router,
   const float* s = scores_in;
   if (s == nullptr) {
     float* buf = scores_out ? scores_out : at<float>(ws, layout(c).scores);
+    if (c.act == MOE_F32) {
+      // fp32 router on the tensor cores: x and w_router as tf32 pairs
+      void* xs = at<void>(ws, layout(c).xs);
+      MOE_TRY(split_rows_f32(x, c.T, c.d, xs, st));
+      MOE_TRY(split_rows_f32(w_router, c.E, c.d, f32_weights(c, ws).wr, st));
+      x = xs;
+      w_router = f32_weights(c, ws).wr;
+    }
     MOE_TRY(router_scores(c, x, w_router, buf, ws, st));
     s = buf;
   } else if (scores_out != nullptr && scores_out != scores_in) {
@@ -158,7 +252,8 @@ moe_status route_stage(const moe_config& c, const void* x, const void* w_router,
 
 moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int32_t* counts, int32_t* offsets,
                          int32_t* sorted_tok, int32_t* slot_pos, const void* x, void* xp, float* xp_scale,
-                         uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st) {
+                         uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st, const float* gate,
+                         float* gate_p, bool pairs) {
   const Layout Lw = layout(c);
   if (c.T == 0) {
     MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), st));
@@ -174,10 +269,12 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
     MOE_CUDA(launch_permute_scatter_e4m3(topk_idx, local_rank, chunk_base, c.T, c.K, c.E,
                                          static_cast<const __nv_bfloat16*>(x), c.d, sorted_tok, slot_pos,
                                          static_cast<uint8_t*>(xp), xp_scale, xq, xq_scale,
-                                         at<float>(ws, Lw.tok_scale), c.expert == MOE_E4M3_UE8M0, num_sms(), st));
+                                         at<float>(ws, Lw.tok_scale), c.expert == MOE_E4M3_UE8M0, num_sms(), st,
+                                         gate, gate_p));
   } else {
-    MOE_CUDA(launch_permute_scatter(topk_idx, local_rank, chunk_base, c.T, c.K, c.E, x, (size_t)c.d * elem_bytes(c.act),
-                                    sorted_tok, slot_pos, xp, num_sms(), st));
+    MOE_CUDA(launch_permute_scatter(topk_idx, local_rank, chunk_base, c.T, c.K, c.E, x,
+                                    (size_t)c.d * elem_bytes(c.act) * (pairs ? 2 : 1), sorted_tok, slot_pos, xp,
+                                    num_sms(), st, gate, gate_p));
   }
   return MOE_OK;
 }
@@ -293,64 +390,48 @@ moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scal
                        const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st) {
   const Layout Lw = layout(c);
   const int TK = c.T * c.K;
-  if (c.act == MOE_F32) {
-    if (routed) {
-      SimtParams p{};
-      p.mode = kSimtSwiGLU;
-      p.A = static_cast<const float*>(xp);
-      p.lda = c.d;
-      p.B = static_cast<const float*>(w->w13);
-      p.groups = c.E;
-      p.offsets = offsets;
-      p.N = c.I;
-      p.Kdim = c.d;
-      p.I = c.I;
-      p.out = at<float>(ws, Lw.h);
-      p.ldo = c.I;
-      MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(TK, c.E), st));
-    }
-    if (shared && c.S > 0) {
-      SimtParams p{};
-      p.mode = kSimtSwiGLU;
-      p.A = static_cast<const float*>(x);
-      p.lda = c.d;
-      p.B = static_cast<const float*>(w->ws13);
-      p.rows = c.T;
-      p.shared = 1;
-      p.N = c.S * c.I;
-      p.Kdim = c.d;
-      p.I = c.I;
-      p.out = at<float>(ws, Lw.hs);
-      p.ldo = c.S * c.I;
-      MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(c.T, 0), st));
-    }
-    return MOE_OK;
-  }
   if (is_f8(c.expert)) {
     return fp8_gemm1(c, xp, xp_scale, offsets, at<uint8_t>(ws, Lw.xq), at<float>(ws, Lw.xq_scale), w, routed,
                      shared, ws, st);
   }
+  // fp32 layers: xp, x and the weights are tf32 pairs (xp and x in the
+  // workspace, the weights from split_weights_f32)
+  const bool f32 = c.act == MOE_F32;
+  const F32W f = f32_weights(c, ws);
   TcGemmLaunch L{};
   L.epi = Epi::kSwiGLU;
+  L.mh = expert_tile_halves(c, routed && !shared);
+  L.split = f32;
   L.bn = 256;
+  const int kbs = f32 ? c.d / 32 : c.d / 64;
   long long tiles = 0;
   if (routed) {
-    MOE_TRY(map_2d(&L.a0, xp, 2, c.d, TK, 64, 128));
-    MOE_TRY(map_3d(&L.b0, w->w13, 2, c.d, 2 * (uint64_t)c.I, c.E, 64, 64));
+    if (f32) {
+      MOE_TRY(map_pairs(&L.a0, xp, c.d, TK, 0, 128));
+      MOE_TRY(map_pairs(&L.b0, f.w13, c.d, 2 * (uint64_t)c.I, c.E, 64));
+    } else {
+      MOE_TRY(map_2d(&L.a0, xp, 2, c.d, TK, 64, 128));
+      MOE_TRY(map_3d(&L.b0, w->w13, 2, c.d, 2 * (uint64_t)c.I, c.E, 64, 64));
+    }
     L.p.groups0 = c.E;
     L.p.offsets0 = offsets;
     L.p.n_tiles0 = c.I / 128;
-    L.p.k_blocks0 = c.d / 64;
+    L.p.k_blocks0 = kbs;
     L.p.out0 = at<void>(ws, Lw.h);
     L.p.ldo0 = c.I;
     tiles += ((long long)TK / 128 + c.E) * L.p.n_tiles0;
   }
   if (shared && c.S > 0) {
-    MOE_TRY(map_2d(&L.a1, x, 2, c.d, c.T, 64, 128));
-    MOE_TRY(map_3d(&L.b1, w->ws13, 2, c.d, 2 * (uint64_t)c.I, c.S, 64, 64));
+    if (f32) {
+      MOE_TRY(map_pairs(&L.a1, x, c.d, c.T, 0, 128));
+      MOE_TRY(map_pairs(&L.b1, f.ws13, c.d, 2 * (uint64_t)c.I, c.S, 64));
+    } else {
+      MOE_TRY(map_2d(&L.a1, x, 2, c.d, c.T, 64, 128));
+      MOE_TRY(map_3d(&L.b1, w->ws13, 2, c.d, 2 * (uint64_t)c.I, c.S, 64, 64));
+    }
     L.p.rows1 = c.T;
     L.p.n_tiles1 = c.S * c.I / 128;
-    L.p.k_blocks1 = c.d / 64;
+    L.p.k_blocks1 = kbs;
     L.p.out1 = at<void>(ws, Lw.hs);
     L.p.ldo1 = c.S * c.I;
     tiles += (long long)((c.T + 127) / 128) * L.p.n_tiles1;
@@ -372,39 +453,49 @@ moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scal
   return MOE_OK;
 }
 
+// Operand maps of a down projection into segment 0 (routed) or 1 (shared):
+// A = h [rows, hk] (fp32 layers: tf32 pairs [rows, 2, hk]), B = the W2 stack
+// [n_mat, d, I] (fp32 layers: its split copy w2s [n_mat, d, 2, I]).
+static moe_status down_maps(const moe_config& c, TcGemmLaunch& L, bool seg1, const void* h, uint64_t hk,
+                            uint64_t rows, const void* w2, const float* w2s, uint64_t n_mat) {
+  CUtensorMap* a = seg1 ? &L.a1 : &L.a0;
+  CUtensorMap* b = seg1 ? &L.b1 : &L.b0;
+  const bool f32 = c.act == MOE_F32;
+  L.split = f32;
+  if (f32) {
+    MOE_TRY(map_pairs(a, h, hk, rows, 0, 128));
+    MOE_TRY(map_pairs(b, w2s, c.I, c.d, n_mat, L.bn));
+  } else {
+    MOE_TRY(map_2d(a, h, 2, hk, rows, 64, 128));
+    MOE_TRY(map_3d(b, w2, 2, c.I, c.d, n_mat, 64, L.bn));
+  }
+  const int kb = (int)(hk / (f32 ? 32 : 64));
+  if (seg1) {
+    L.p.k_blocks1 = kb;
+    L.a0 = L.a1;
+    L.b0 = L.b1;
+  } else {
+    L.p.k_blocks0 = kb;
+    L.a1 = L.a0;
+    L.b1 = L.b0;
+  }
+  return MOE_OK;
+}
+
 // GEMM2 of the routed experts: yp = h W2^T (not gate-scaled).
 moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, void* yp, void* ws,
                               cudaStream_t st) {
   const Layout Lw = layout(c);
   const int TK = c.T * c.K;
-  if (c.act == MOE_F32) {
-    SimtParams p{};
-    p.mode = kSimtStore;
-    p.A = at<float>(ws, Lw.h);
-    p.lda = c.I;
-    p.B = static_cast<const float*>(w->w2);
-    p.groups = c.E;
-    p.offsets = offsets;
-    p.N = c.d;
-    p.Kdim = c.I;
-    p.I = c.I;
-    p.out = static_cast<float*>(yp);
-    p.ldo = c.d;
-    MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(TK, c.E), st));
-    return MOE_OK;
-  }
   if (is_f8(c.expert)) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
   TcGemmLaunch L{};
-  L.epi = Epi::kStore;
+  L.epi = c.act == MOE_F32 ? Epi::kStoreF32 : Epi::kStore;
+  L.mh = expert_tile_halves(c, false);
   L.bn = down_bn(c.d);
-  MOE_TRY(map_2d(&L.a0, at<void>(ws, Lw.h), 2, c.I, TK, 64, 128));
-  MOE_TRY(map_3d(&L.b0, w->w2, 2, c.I, c.d, c.E, 64, L.bn));
-  L.a1 = L.a0;
-  L.b1 = L.b0;
+  MOE_TRY(down_maps(c, L, false, at<void>(ws, Lw.h), c.I, TK, w->w2, f32_weights(c, ws).w2, c.E));
   L.p.groups0 = c.E;
   L.p.offsets0 = offsets;
   L.p.n_tiles0 = c.d / L.bn;
-  L.p.k_blocks0 = c.I / 64;
   L.p.out0 = yp;
   L.p.ldo0 = c.d;
   L.p.I = c.I;
@@ -415,59 +506,97 @@ moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const
   return MOE_OK;
 }
 
+moe_status shared_seed_stage(const moe_config& c, const moe_weights* w, float* acc, void* ws, cudaStream_t st) {
+  if (c.S == 0) {
+    MOE_CUDA(cudaMemsetAsync(acc, 0, sizeof(float) * (size_t)c.T * c.d, st));
+    return MOE_OK;
+  }
+  const Layout Lw = layout(c);
+  TcGemmLaunch L{};
+  L.epi = Epi::kStoreF32;
+  L.mh = expert_tile_halves(c, false);
+  L.bn = down_bn(c.d);
+  MOE_TRY(down_maps(c, L, true, at<void>(ws, Lw.hs), (uint64_t)c.S * c.I, c.T, w->ws2, f32_weights(c, ws).ws2,
+                    c.S));
+  L.p.groups0 = 0;
+  L.p.rows1 = c.T;
+  L.p.n_tiles1 = c.d / L.bn;
+  L.p.out1 = acc;
+  L.p.ldo1 = c.d;
+  L.p.I = c.I;
+  L.p.err = at<int>(ws, 0);
+  L.grid = tc_grid((long long)((c.T + 127) / 128) * L.p.n_tiles1);
+  L.stream = st;
+  MOE_CUDA(launch_tc_gemm(L));
+  return MOE_OK;
+}
+
+moe_status gemm2_scatter_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, float* acc,
+                               void* ws, cudaStream_t st) {
+  const Layout Lw = layout(c);
+  const int TK = c.T * c.K;
+  TcGemmLaunch L{};
+  L.epi = Epi::kScatterAdd;
+  L.mh = expert_tile_halves(c, false);
+  L.bn = down_bn(c.d);
+  MOE_TRY(down_maps(c, L, false, at<void>(ws, Lw.h), c.I, TK, w->w2, f32_weights(c, ws).w2, c.E));
+  L.p.groups0 = c.E;
+  L.p.offsets0 = offsets;
+  L.p.n_tiles0 = c.d / L.bn;
+  L.p.out0 = acc;
+  L.p.ldo0 = c.d;
+  L.p.I = c.I;
+  L.p.sorted_tok = at<int>(ws, Lw.sorted_tok);
+  L.p.gate_p = at<float>(ws, Lw.gate_p);
+  L.p.err = at<int>(ws, 0);
+  L.grid = tc_grid(((long long)TK / 128 + c.E) * L.p.n_tiles0);
+  L.stream = st;
+  MOE_CUDA(launch_tc_gemm(L));
+  return MOE_OK;
+}
+
+moe_status acc_round_stage(const moe_config& c, const float* acc, void* out, cudaStream_t st) {
+  MOE_CUDA(launch_acc_to_bf16(acc, (size_t)c.T * c.d, out, num_sms(), st));
+  return MOE_OK;
+}
+
 // Shared experts' down projection with the gate-weighted routed rows added in
 // its epilogue (or a plain gather-sum when there are no shared experts).
 moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_t* slot_pos, const float* gate,
                                const moe_weights* w, void* out, void* ws, cudaStream_t st) {
   const Layout Lw = layout(c);
+  const bool f32 = c.act == MOE_F32;
   if (c.S == 0) {
-    if (c.act == MOE_BF16) {
-      MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, out, num_sms(), st));
-    } else {
+    if (f32) {
       MOE_CUDA(launch_gather_combine(yp, slot_pos, gate, c.T, c.d, c.K, false, out, num_sms(), st));
+    } else {
+      MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, out, num_sms(), st));
     }
-    return MOE_OK;
-  }
-  if (c.act == MOE_F32) {
-    SimtParams p{};
-    p.mode = kSimtCombine;
-    p.A = at<float>(ws, Lw.hs);
-    p.lda = c.S * c.I;
-    p.B = static_cast<const float*>(w->ws2);
-    p.rows = c.T;
-    p.shared = 1;
-    p.N = c.d;
-    p.Kdim = c.S * c.I;
-    p.I = c.I;
-    p.out = static_cast<float*>(out);
-    p.ldo = c.d;
-    p.slot_pos = slot_pos;
-    p.gate = gate;
-    p.yp = static_cast<const float*>(yp);
-    p.topk = c.K;
-    MOE_CUDA(launch_simt_gemm(p, simt_max_mtiles(c.T, 0), st));
     return MOE_OK;
   }
   // routed sum r[t] (in the xp region of the workspace: the permuted rows are
   // dead once the routed GEMM1 has run), added by the down projection's epilogue
   void* r = at<void>(ws, Lw.xp);
-  MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, r, num_sms(), st));
+  if (f32) {
+    MOE_CUDA(launch_gather_combine(yp, slot_pos, gate, c.T, c.d, c.K, false, r, num_sms(), st));
+  } else {
+    MOE_CUDA(launch_routed_sum_bf16(yp, slot_pos, gate, c.T, c.d, c.K, r, num_sms(), st));
+  }
   if (is_f8(c.expert)) return fp8_gemm2(c, nullptr, w, nullptr, true, r, out, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kCombine;
+  L.mh = expert_tile_halves(c, false);
   L.bn = down_bn(c.d);
-  MOE_TRY(map_2d(&L.a1, at<void>(ws, Lw.hs), 2, (uint64_t)c.S * c.I, c.T, 64, 128));
-  MOE_TRY(map_3d(&L.b1, w->ws2, 2, c.I, c.d, c.S, 64, L.bn));
-  L.a0 = L.a1;
-  L.b0 = L.b1;
+  MOE_TRY(down_maps(c, L, true, at<void>(ws, Lw.hs), (uint64_t)c.S * c.I, c.T, w->ws2, f32_weights(c, ws).ws2,
+                    c.S));
   L.p.groups0 = 0;
   L.p.rows1 = c.T;
   L.p.n_tiles1 = c.d / L.bn;
-  L.p.k_blocks1 = c.S * c.I / 64;
   L.p.out1 = out;
   L.p.ldo1 = c.d;
   L.p.I = c.I;
   L.p.radd = static_cast<const __nv_bfloat16*>(r);
+  L.p.radd_f32 = static_cast<const float*>(r);
   L.p.err = at<int>(ws, 0);
   L.grid = tc_grid((long long)((c.T + 127) / 128) * L.p.n_tiles1);
   L.stream = st;

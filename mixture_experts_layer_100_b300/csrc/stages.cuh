@@ -34,10 +34,19 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline bool is_f8(moe_dtype t) { return t == MOE_E4M3 || t == MOE_E4M3_UE8M0; }
 
+// moe_layer_forward combines by fp32 reductions in the routed down
+// projection's epilogue (bf16 or fp32 layers; not the FP8 expert GEMMs).
+inline bool scatter_combine(const moe_config& c) {
+  return c.combine == MOE_COMBINE_SCATTER_ADD && c.act == c.expert;
+}
+
 // ------------------------------------------------------------ workspace
 struct Layout {
   size_t err, scores, local_rank, chunk_hist, chunk_base, offsets, sorted_tok, slot_pos;
-  size_t xp, xp_scale, xq, xq_scale, tok_scale, h, h_scale, hs, hs_scale, yp, total;
+  size_t xp, xp_scale, xq, xq_scale, tok_scale, h, h_scale, hs, hs_scale, yp, gate_p, acc;
+  // fp32 layers: x and the weights as tf32 pairs (see F32W)
+  size_t xs, wr_s, w13_s, w2_s, ws13_s, ws2_s;
+  size_t total;
 };
 
 Layout layout(const moe_config& c);
@@ -49,6 +58,21 @@ P* at(void* ws, size_t off) {
 
 int num_sms();
 
+// ---- fp32 layers: every GEMM operand as tf32 pairs ([rows, 2, K]: the tf32
+// high parts of a row, then the remainders), multiplied as hi*hi + hi*lo +
+// lo*hi on the tensor cores (kind::tf32, fp32 accumulation).
+struct F32W {
+  float *wr, *w13, *w2, *ws13, *ws2;  // [E,2,d], [E,2I,2,d], [E,d,2,I], [S,2I,2,d], [S,d,2,I]
+};
+F32W f32_weights(const moe_config& c, void* ws);
+// Splits the weights named by the flags into the workspace.
+moe_status split_weights_f32(const moe_config& c, const moe_weights* w, bool router, bool routed, bool shared,
+                             void* ws, cudaStream_t st);
+// fp32 rows [rows, cols] -> tf32 pairs [rows, 2, cols].
+moe_status split_rows_f32(const void* src, long long rows, int cols, void* dst, cudaStream_t st);
+
+// Router GEMM + sigmoid, scores s [T, E]. For fp32 layers x and w_router are
+// the tf32 pairs (ws xs, F32W::wr).
 moe_status router_scores(const moe_config& c, const void* x, const void* w_router, float* s, void* ws,
                          cudaStream_t st);
 moe_status route_stage(const moe_config& c, const void* x, const void* w_router, const float* scores_in,
@@ -56,11 +80,19 @@ moe_status route_stage(const moe_config& c, const void* x, const void* w_router,
                        void* ws, cudaStream_t st);
 moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int32_t* counts, int32_t* offsets,
                          int32_t* sorted_tok, int32_t* slot_pos, const void* x, void* xp, float* xp_scale,
-                         uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st);
+                         uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st, const float* gate = nullptr,
+                         float* gate_p = nullptr, bool pairs = false);
 moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
                        const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st);
 moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, void* yp, void* ws,
                               cudaStream_t st);
+// Scatter-add combine: the shared experts' down projection writes the fp32
+// accumulator (zeros when S = 0); the routed down projection adds gate * row
+// into it; the accumulator is rounded to bf16 out.
+moe_status shared_seed_stage(const moe_config& c, const moe_weights* w, float* acc, void* ws, cudaStream_t st);
+moe_status gemm2_scatter_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, float* acc,
+                               void* ws, cudaStream_t st);
+moe_status acc_round_stage(const moe_config& c, const float* acc, void* out, cudaStream_t st);
 moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_t* slot_pos, const float* gate,
                                const moe_weights* w, void* out, void* ws, cudaStream_t st);
 

@@ -55,6 +55,7 @@ class Preset:
     gamma: float = 1e-3
     group_topk: int = 2
     seed: int = 0
+    combine: str = "gather"  # how the layer call combines the routed rows: "gather" or "scatter_add"
 
     def replace(self, **kw) -> "Preset":
         return dataclasses.replace(self, **kw)

@@ -42,9 +42,12 @@ def small_preset(name, **over):
     return BASE.replace(name=name, zipf=False, bias="u0.01", **kw)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("combine", ["gather", "scatter_add"])
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_layer_bf16_all_tokens(name):
-    p = small_preset(name)
+def test_small_layer_all_tokens(name, combine, dtype):
+    """bf16 layers, and fp32 layers (tf32-pair tensor-core GEMMs, 1e-5)."""
+    p = small_preset(name, combine=combine, dtype=dtype, expert_dtype=dtype)
     w = synth.make_weights(p)
     x = synth.make_x(p, w.w_router)
     b = synth.make_bias(p)
@@ -75,9 +78,10 @@ def test_tiny_fp32_preset_with_bias_steps():
         np.testing.assert_array_equal(bd.cpu().numpy(), b_ref)
 
 
-def test_all_tokens_on_four_experts():
+@pytest.mark.parametrize("combine", ["gather", "scatter_add"])
+def test_all_tokens_on_four_experts(combine):
     """Bias +1 on group 0: every token takes its four experts (4 x T rows)."""
-    p = small_preset("t300_d256_e16_i256", T=1000)
+    p = small_preset("t300_d256_e16_i256", T=1000, combine=combine)
     w = synth.make_weights(p)
     x = synth.make_x(p, w.w_router)
     b = torch.zeros(p.E)
@@ -101,8 +105,9 @@ def test_zero_router_all_ties():
     compare(p, res, oracle_rows(p, w, x, b), b)
 
 
-def test_zero_routed_weights_give_shared_only():
-    p = small_preset("t515_d384_e32_i384_s2")
+@pytest.mark.parametrize("combine", ["gather", "scatter_add"])
+def test_zero_routed_weights_give_shared_only(combine):
+    p = small_preset("t515_d384_e32_i384_s2", combine=combine)
     w = synth.make_weights(p, zero_routed=True)
     x = synth.make_x(p, w.w_router)
     b = synth.make_bias(p)
@@ -178,6 +183,25 @@ def test_entry_points_compose_to_the_layer():
         assert np.abs(got - ref).max() / np.abs(ref).max() <= 2e-2
 
 
+def test_scatter_add_combine_matches_gather():
+    """The two combine modes compute the same sums in a different order: they
+    agree to fp32 rounding of K gated rows (before the bf16 output rounding),
+    and the routing, loads and bias are identical."""
+    p = small_preset("t515_d384_e32_i384_s2")
+    w = synth.make_weights(p)
+    wd = device_weights(w)
+    x = synth.make_x(p, w.w_router).to(DEV)
+    b0 = synth.make_bias(p).to(DEV)
+    bg, bs = b0.clone(), b0.clone()
+    rg = run_layer(p, wd, x, bg, gamma=p.gamma)
+    rs = run_layer(p.replace(combine="scatter_add"), wd, x, bs, gamma=p.gamma)
+    for k in ("topk_idx", "topk_gate", "counts"):
+        assert torch.equal(rg[k], rs[k])
+    assert torch.equal(bg, bs)
+    og, os_ = rg["out"].float(), rs["out"].float()
+    assert (og - os_).abs().max().item() <= 2 ** -7 * og.abs().max().item()
+
+
 def test_layer_is_deterministic():
     p = small_preset("t515_d384_e32_i384_s2")
     w = synth.make_weights(p)
@@ -226,14 +250,15 @@ def v3_weights():
     torch.cuda.empty_cache()
 
 
-def test_v3_preset_full_size(v3_weights):
+@pytest.mark.parametrize("combine", ["gather", "scatter_add"])
+def test_v3_preset_full_size(v3_weights, combine):
     """The bench workload (T = 16384, V3 shape, skewed routing): routing of
     every token bit-exact against the oracle given the library's own scores,
     and the layer output element by element on a 1024-token sample that
     reaches every expert's first and last permuted row and every tile of the
     three hottest experts."""
     from oracle import cpp
-    p = synth.PRESETS["v3_t16384_d7168_e256_bf16"]
+    p = synth.PRESETS["v3_t16384_d7168_e256_bf16"].replace(combine=combine)
     w = v3_weights
     x = synth.make_x(p, w.w_router, device=DEV)
     b = synth.make_bias(p)
