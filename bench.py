@@ -457,19 +457,23 @@ def run_graph_replay(step, p, K, dev, world):
 
 
 def kernels_per_step(p):
-    """Kernels of this library one moe_layer_forward step launches."""
-    if p.dtype == "f32":
-        # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, combine, bias update
-        return 10 - (1 if p.S == 0 else 0)
-    n = 11  # router, select, rank, scan, scatter, shared gemm1, gemm1, gemm2, routed sum, combine, bias update
-    if p.combine == "scatter_add" and p.expert_dtype == "bf16":
-        # router, select, rank, scan, scatter, shared gemm1, shared down projection (fp32 seed), gemm1,
-        # gemm2 with the scatter-add, rounding pass, bias update; S = 0: no shared GEMMs (a memset seeds)
-        return 11 if p.S > 0 else 9
-    if p.S == 0:
-        n -= 2  # no shared gemm1; the routed sum writes the output
-    if p.expert_dtype in ("e4m3", "e4m3_ue8m0"):
+    """Kernels of this library one moe_layer_forward step launches (cudaMemset
+    calls are not counted)."""
+    f8 = p.expert_dtype in ("e4m3", "e4m3_ue8m0")
+    scatter = p.combine == "scatter_add" and not f8
+    n = 6  # router, selection, rank, scan, scatter, bias update
+    n += 1  # routed GEMM1
+    if p.S > 0:
+        n += 1  # shared experts' GEMM1 (side stream)
+    if scatter:
+        n += 1 + (1 if p.S > 0 else 0)  # routed GEMM2 with the reductions; shared down projection (fp32 seed)
+        n += 1 if p.dtype == "bf16" else 0  # rounding pass (fp32 layers add into out itself)
+    else:
+        n += 2 + (1 if p.S > 0 else 0)  # routed GEMM2, routed sum; shared down projection with the sum added
+    if f8:
         n += 1 + (1 if p.S > 0 else 0)  # tile-major scale layout; x quantised for the shared experts
+    if p.dtype == "f32":
+        n += 4 + (2 if p.S > 0 else 0)  # x, router, routed and shared weights split into tf32 pairs
     return n
 
 

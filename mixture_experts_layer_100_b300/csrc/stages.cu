@@ -134,25 +134,19 @@ static moe_status map_pairs(CUtensorMap* m, const void* ptr, uint64_t K, uint64_
 
 static int down_bn(int d) { return d % 256 == 0 ? 256 : 128; }
 
-// 128-row halves per tile of the bf16 routed experts' GEMM1: 2 (256-row tiles
-// whose halves share each staged weight slice, a third less operand traffic
-// from L2) when the experts average at least two full 128-row tiles, else 1
-// (256-row tiles stage fewer K slices, which starves the weight-streaming
-// decode shapes). The other expert GEMMs measured faster with 1.
-// MOE_GEMM_TILE_ROWS=128 or 256 forces one size for every expert GEMM (read
-// once per process; a switch for comparisons, results are identical).
-static int forced_tile_halves() {
-  static int mh = -1;
-  if (mh < 0) {
+// 128-row halves per tile of the bf16 expert GEMMs: 1 by default;
+// MOE_GEMM_TILE_ROWS=256 selects 256-row tiles whose two halves share each
+// staged weight slice (a third less operand traffic from L2, but a single
+// TMEM accumulator, so the epilogue no longer overlaps the next tile's main
+// loop; measured slower on every workload here). Read once per process; the
+// two tilings give bit-identical results.
+static int expert_tile_halves() {
+  static int mh = 0;
+  if (mh == 0) {
     const char* v = getenv("MOE_GEMM_TILE_ROWS");
-    mh = v == nullptr ? 0 : atoi(v) == 128 ? 1 : atoi(v) == 256 ? 2 : 0;
+    mh = (v != nullptr && atoi(v) == 256) ? 2 : 1;
   }
   return mh;
-}
-
-static int expert_tile_halves(const moe_config& c, bool routed_gemm1) {
-  if (forced_tile_halves() != 0) return forced_tile_halves();
-  return routed_gemm1 && (long long)c.T * c.K >= 256LL * c.E ? 2 : 1;
 }
 
 static int router_bn(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
@@ -400,7 +394,7 @@ moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scal
   const F32W f = f32_weights(c, ws);
   TcGemmLaunch L{};
   L.epi = Epi::kSwiGLU;
-  L.mh = expert_tile_halves(c, routed && !shared);
+  L.mh = expert_tile_halves();
   L.split = f32;
   L.bn = 256;
   const int kbs = f32 ? c.d / 32 : c.d / 64;
@@ -490,7 +484,7 @@ moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const
   if (is_f8(c.expert)) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
   TcGemmLaunch L{};
   L.epi = c.act == MOE_F32 ? Epi::kStoreF32 : Epi::kStore;
-  L.mh = expert_tile_halves(c, false);
+  L.mh = expert_tile_halves();
   L.bn = down_bn(c.d);
   MOE_TRY(down_maps(c, L, false, at<void>(ws, Lw.h), c.I, TK, w->w2, f32_weights(c, ws).w2, c.E));
   L.p.groups0 = c.E;
@@ -514,7 +508,7 @@ moe_status shared_seed_stage(const moe_config& c, const moe_weights* w, float* a
   const Layout Lw = layout(c);
   TcGemmLaunch L{};
   L.epi = Epi::kStoreF32;
-  L.mh = expert_tile_halves(c, false);
+  L.mh = expert_tile_halves();
   L.bn = down_bn(c.d);
   MOE_TRY(down_maps(c, L, true, at<void>(ws, Lw.hs), (uint64_t)c.S * c.I, c.T, w->ws2, f32_weights(c, ws).ws2,
                     c.S));
@@ -537,7 +531,7 @@ moe_status gemm2_scatter_stage(const moe_config& c, const int32_t* offsets, cons
   const int TK = c.T * c.K;
   TcGemmLaunch L{};
   L.epi = Epi::kScatterAdd;
-  L.mh = expert_tile_halves(c, false);
+  L.mh = expert_tile_halves();
   L.bn = down_bn(c.d);
   MOE_TRY(down_maps(c, L, false, at<void>(ws, Lw.h), c.I, TK, w->w2, f32_weights(c, ws).w2, c.E));
   L.p.groups0 = c.E;
@@ -585,7 +579,7 @@ moe_status gemm2_combine_stage(const moe_config& c, const void* yp, const int32_
   if (is_f8(c.expert)) return fp8_gemm2(c, nullptr, w, nullptr, true, r, out, ws, st);
   TcGemmLaunch L{};
   L.epi = Epi::kCombine;
-  L.mh = expert_tile_halves(c, false);
+  L.mh = expert_tile_halves();
   L.bn = down_bn(c.d);
   MOE_TRY(down_maps(c, L, true, at<void>(ws, Lw.hs), (uint64_t)c.S * c.I, c.T, w->ws2, f32_weights(c, ws).ws2,
                     c.S));
