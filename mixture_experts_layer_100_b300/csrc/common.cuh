@@ -38,6 +38,10 @@ __device__ __forceinline__ int read_error(const int* err) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// silu with the hardware exp2 and reciprocal approximations (a few fp32 ulp,
+// far below the bf16 / e4m3 rounding of the SwiGLU output h).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 // Scale of one e4m3 tile whose largest magnitude is amax; 1 for an all-zero
 // tile. The fp32 rule is amax / 448. The UE8M0 rule is the smallest power of
 // two 2^e >= amax / 448 with e clamped to [-127, 127] (the exponents a UE8M0

@@ -121,7 +121,7 @@ __device__ __forceinline__ void tile_epilogue(const TcGemmParams& p, const Tile&
       ptx::tmem_ld32(tbase + gcol, v);
       ptx::tmem_ld32(tbase + gcol + 64, u);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * u[j];
+      for (int j = 0; j < 32; ++j) v[j] = silu_fast(v[j]) * u[j];
       pack_bf16x32(v, w);
       warp_store_rows64(stg, threadIdx.x & 31, w, base + c * 64, (size_t)ldo * 2, nrows);
     }

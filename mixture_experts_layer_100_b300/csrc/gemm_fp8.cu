@@ -57,10 +57,7 @@ __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 epilogue warps (SwiGLU)
 }
 
-// silu with the hardware exp2 and reciprocal approximations (a few ulp of
-// fp32, far below the e4m3 step of h): the SwiGLU tail of a tile runs while
-// the tensor core can work at most two K blocks ahead, so its length counts.
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   return (uint32_t)f32_to_e4m3(a) | ((uint32_t)f32_to_e4m3(b) << 8) | ((uint32_t)f32_to_e4m3(c) << 16) |

@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc[j] = silu(acc[j]) * acc[64 + j];
+          acc[j] = silu_fast(acc[j]) * acc[64 + j];
           amax = fmaxf(amax, fabsf(acc[j]));
         }
         s_amax[half * 128 + r_in_tile] = amax;
