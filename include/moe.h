@@ -80,9 +80,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E4M3_UE8M0 = 3 } moe
  * MOE_COMBINE_SCATTER_ADD: the shared experts' down projection writes an fp32
  *   [T, d] accumulator, the routed down projection's epilogue adds gate * row
  *   into it with fp32 reductions (red.global.add), and one pass rounds it to
- *   the output dtype. The order of the K fp32 adds per element is not fixed,
- *   so outputs may differ in the last bits from call to call. bf16 layers
- *   only; fp32 layers always gather. */
+ *   the output dtype (fp32 layers accumulate in out itself). The order of
+ *   the K fp32 adds per element is not fixed, so outputs may differ in the
+ *   last bits from call to call. bf16 and fp32 layers; layers with FP8
+ *   expert GEMMs always gather. */
 typedef enum { MOE_COMBINE_GATHER = 0, MOE_COMBINE_SCATTER_ADD = 1 } moe_combine_mode;
 
 typedef struct {
@@ -118,8 +119,11 @@ typedef struct {
 /* Bytes of device workspace that every call below needs for `cfg`
  * (moe_layer_forward needs the most; one buffer of this size serves all).
  * Limits checked here and by every call: E <= 512 with E % G == 0, G <= 32,
- * 1 <= group_topk <= E/G, K <= 32, K <= M * (E/G), M <= G; for act BF16
- * d % 128 == 0, I % 128 == 0 and E <= 256. */
+ * 1 <= group_topk <= E/G, K <= 32, K <= M * (E/G), M <= G, d % 128 == 0 and
+ * I % 128 == 0; for act BF16 also E <= 256. fp32 layers (act MOE_F32) run
+ * their GEMMs on the tensor cores with each fp32 operand split into a tf32
+ * pair (high part + remainder; hi*hi + hi*lo + lo*hi), the pairs kept in the
+ * workspace (x and the weights are split at the start of every call). */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Router and routing [digest-2.2], [resmic-moe].
