@@ -33,6 +33,7 @@ SMALL = {
     "t333_d256_e32_nodesum": dict(T=333, d=256, E=32, G=4, K=4, M=2, I=128, S=1, group_topk=8),
     "t150_d256_e64_k16": dict(T=150, d=256, E=64, G=4, K=16, M=2, I=128, S=1),
     "t90_d256_e64_k32": dict(T=90, d=256, E=64, G=2, K=32, M=1, I=128, S=1),
+    "t257_d256_e32_k1": dict(T=257, d=256, E=32, G=4, K=1, M=1, I=128, S=1),   # top-1 routing, one group
 }
 
 
@@ -76,6 +77,20 @@ def test_tiny_fp32_preset_with_bias_steps():
         compare(p, res, ref, b_ref, max_flip=0.0)
         b_ref = om.bias_update(om.expert_counts(ref["topk_idx"], p.E), b_ref, p.gamma, p.T, p.K)
         np.testing.assert_array_equal(bd.cpu().numpy(), b_ref)
+
+
+@pytest.mark.parametrize("combine", ["gather", "scatter_add"])
+def test_fp32_layer_with_512_experts(combine):
+    """The largest expert count (fp32 layers only): the router runs two
+    256-column tiles and the grouped GEMMs walk 512 groups."""
+    p = small_preset("t300_d256_e16_i256", T=400, d=128, E=512, G=32, K=8, M=4, I=128, S=1, combine=combine,
+                     dtype="f32", expert_dtype="f32")
+    w = synth.make_weights(p)
+    x = synth.make_x(p, w.w_router)
+    b = synth.make_bias(p)
+    res = run_layer(p, device_weights(w), x.to(DEV), b.to(DEV))
+    compare(p, res, oracle_rows(p, w, x, b), b)
+    assert res["counts"].sum().item() == p.T * p.K
 
 
 @pytest.mark.parametrize("combine", ["gather", "scatter_add"])
