@@ -815,7 +815,8 @@ def run_ours(a, p):
         cpu = run_cpu_baseline(p, w, x)
 
     extra = None
-    if rank == 0 and world == 1 and not a.no_extra and p.name == DEFAULT_PRESET:
+    if rank == 0 and world == 1 and not a.no_extra and p == synth.PRESETS[DEFAULT_PRESET]:
+        # only for the unmodified headline workload: the other configurations reuse its V3 weights
         del ws
         torch.cuda.empty_cache()
         extra = {"combine_ab": run_combine_ab(B, p, w, x, dev)}
