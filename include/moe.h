@@ -233,6 +233,26 @@ moe_status moe_quantize_weights_e4m3_ue8m0(const void* w, int n_mat, int rows, i
 moe_status moe_seq_balance(const moe_config* cfg, const float* scores, const int32_t* topk_idx, int seq_len,
                            float alpha, float* loss, float* f, float* p, void* ws, moe_stream_t stream);
 
+/* Row moves for expert-parallel dispatch and combine [digest-3.3: tokens are
+ * sent to the GPUs that hold their experts and the expert outputs are sent
+ * back]. A rank's moe_permute output is already ordered by destination rank
+ * (experts are placed in contiguous blocks per rank), and the rows it receives
+ * arrive source-major; these two calls reorder them for the rank's grouped
+ * expert GEMMs and back:
+ *   moe_gather_rows:  dst[i] = src[idx[i]] for i < n (src holds n_src rows);
+ *   moe_scatter_rows: dst[idx[i]] = src[i] for i < n (dst holds n_dst rows).
+ * Rows are row_bytes long (a multiple of 4), src and dst 16-byte aligned
+ * device buffers owned by the caller, idx [n] int32 on the device. An index
+ * outside the other buffer's rows is skipped and reported as code 0x203 in
+ * the error word of ws (any workspace of moe_workspace_size bytes; read it
+ * with moe_device_error). A scatter index that repeats leaves one of the
+ * rows written to it, which one unspecified. n == 0 is a no-op. Asynchronous
+ * on stream. MOE_ERR_INVALID_ARG for bad pointers or sizes. */
+moe_status moe_gather_rows(const void* src, int n_src, const int32_t* idx, int n, size_t row_bytes, void* dst,
+                           void* ws, moe_stream_t stream);
+moe_status moe_scatter_rows(const void* src, const int32_t* idx, int n, size_t row_bytes, void* dst, int n_dst,
+                            void* ws, moe_stream_t stream);
+
 /* Bytes of the fixed device array that moe_permute_static uses as scratch. */
 #define MOE_PERMUTE_STATIC_SCRATCH_BYTES (4u << 20)
 

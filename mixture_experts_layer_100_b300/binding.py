@@ -65,6 +65,8 @@ _SIGS = {
     "moe_quantize_weights_e4m3_ue8m0": [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P],
     "moe_permute_static": [ctypes.POINTER(moe_config)] + [_P] * 7 + [_P],
     "moe_seq_balance": [ctypes.POINTER(moe_config), _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, _P],
+    "moe_gather_rows": [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_size_t, _P, _P, _P],
+    "moe_scatter_rows": [_P, _P, ctypes.c_int, ctypes.c_size_t, _P, ctypes.c_int, _P, _P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_selftest_timeout": [_P, _P],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
@@ -185,6 +187,22 @@ def moe_seq_balance(cfg, scores, topk_idx, seq_len: int, alpha: float, loss, f=N
     _check("moe_seq_balance", lib.moe_seq_balance(
         ctypes.byref(cfg), _ptr(scores), _ptr(topk_idx), int(seq_len), ctypes.c_float(alpha), _ptr(loss), _ptr(f),
         _ptr(p), _ptr(ws), _stream(stream)))
+
+
+def _row_bytes(t: torch.Tensor) -> int:
+    return t[0].numel() * t.element_size() if t.shape[0] else t.element_size()
+
+
+def moe_gather_rows(src, idx, dst, ws, stream=None):
+    """dst[i] = src[idx[i]] (rows); idx int32 on the device."""
+    _check("moe_gather_rows", lib.moe_gather_rows(_ptr(src), src.shape[0], _ptr(idx), idx.numel(), _row_bytes(dst),
+                                                  _ptr(dst), _ptr(ws), _stream(stream)))
+
+
+def moe_scatter_rows(src, idx, dst, ws, stream=None):
+    """dst[idx[i]] = src[i] (rows); idx int32 on the device."""
+    _check("moe_scatter_rows", lib.moe_scatter_rows(_ptr(src), _ptr(idx), idx.numel(), _row_bytes(src), _ptr(dst),
+                                                    dst.shape[0], _ptr(ws), _stream(stream)))
 
 
 def moe_set_stage_events(events) -> None:

@@ -299,6 +299,28 @@ moe_status moe_seq_balance(const moe_config* cfg, const float* scores, const int
   return MOE_OK;
 }
 
+static moe_status move_rows(const void* src, const int32_t* idx, int n, int n_other, size_t row_bytes, void* dst,
+                            bool gather, void* ws, moe_stream_t stream) {
+  if (n < 0 || n_other < 0 || row_bytes == 0 || row_bytes % 4 != 0 || row_bytes / 4 > 0x7fffffffu ||
+      ws == nullptr || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!ok_ptr(src) || !ok_ptr(dst) || !ok_ptr(idx)) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_move_rows(src, idx, n, n_other, row_bytes, dst, gather, static_cast<int*>(ws), num_sms(),
+                            reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_gather_rows(const void* src, int n_src, const int32_t* idx, int n, size_t row_bytes, void* dst,
+                           void* ws, moe_stream_t stream) {
+  return move_rows(src, idx, n, n_src, row_bytes, dst, true, ws, stream);
+}
+
+moe_status moe_scatter_rows(const void* src, const int32_t* idx, int n, size_t row_bytes, void* dst, int n_dst,
+                            void* ws, moe_stream_t stream) {
+  return move_rows(src, idx, n, n_dst, row_bytes, dst, false, ws, stream);
+}
+
 moe_status moe_set_stage_events(void* const* events, int count) {
   if (count == 0) {
     g_stage_on = false;

@@ -18,6 +18,7 @@ enum DevErr : int {
   kDevTimeoutSelfTest = 0x105,   // moe_selftest_timeout: the wait ran out as intended
   kDevBadExpertIndex = 0x201,    // topk_idx entry outside [0, E)
   kDevCountMismatch = 0x202,     // counts[] is not the histogram of topk_idx
+  kDevBadRowIndex = 0x203,       // moe_gather_rows / moe_scatter_rows: row index out of range
 };
 
 // A device-side wait that sees no progress for this long gives up.

@@ -31,6 +31,12 @@ cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_ra
                                         bool ue8m0, int num_sms, cudaStream_t st, const float* gate_in = nullptr,
                                         float* gate_p = nullptr);
 
+// Rows moved by an index list (row_bytes a multiple of 4): gather dst[i] =
+// src[idx[i]] (n_other = rows of src) or scatter dst[idx[i]] = src[i]
+// (n_other = rows of dst); out-of-range indices are skipped and reported.
+cudaError_t launch_move_rows(const void* src, const int* idx, int n, int n_other, size_t row_bytes, void* dst,
+                             bool gather, int* err, int num_sms, cudaStream_t st);
+
 // ---- bias update and quantisers (bias_quant.cu)
 cudaError_t launch_bias_update(const int* counts, int E, long long TK, float gamma, float* bias,
                                float* max_over_mean, cudaStream_t st);

@@ -260,7 +260,54 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Row moves by an index list (the receive-side reorder of expert-parallel
+// dispatch and its inverse): one warp per row, 16-byte (or 4-byte) vectors.
+// gather: dst[i] = src[idx[i]]; scatter: dst[idx[i]] = src[i]. An index
+// outside [0, n_other) is skipped and reported in err.
+template <typename VecT, bool GATHER>
+__global__ void __launch_bounds__(kWarps * 32)
+    move_rows_kernel(const VecT* __restrict__ src, const int* __restrict__ idx, int n, int n_other, int row_vecs,
+                     VecT* __restrict__ dst, int* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = blockIdx.x * kWarps + warp; i < n; i += gridDim.x * kWarps) {
+    const int j = idx[i];
+    if (j < 0 || j >= n_other) {
+      if (lane == 0) set_error(err, kDevBadRowIndex);
+      continue;
+    }
+    const VecT* s = src + (size_t)(GATHER ? j : i) * row_vecs;
+    VecT* d = dst + (size_t)(GATHER ? i : j) * row_vecs;
+    for (int c = lane; c < row_vecs; c += 32) d[c] = s[c];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_move_rows(const void* src, const int* idx, int n, int n_other, size_t row_bytes, void* dst,
+                             bool gather, int* err, int num_sms, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int blocks = std::max(1, std::min((n + kWarps - 1) / kWarps, num_sms * 8));
+  if (row_bytes % 16 == 0) {
+    const int rv = (int)(row_bytes / 16);
+    auto s = static_cast<const uint4*>(src);
+    auto d = static_cast<uint4*>(dst);
+    if (gather) {
+      move_rows_kernel<uint4, true><<<blocks, kWarps * 32, 0, st>>>(s, idx, n, n_other, rv, d, err);
+    } else {
+      move_rows_kernel<uint4, false><<<blocks, kWarps * 32, 0, st>>>(s, idx, n, n_other, rv, d, err);
+    }
+  } else {
+    const int rv = (int)(row_bytes / 4);
+    auto s = static_cast<const uint32_t*>(src);
+    auto d = static_cast<uint32_t*>(dst);
+    if (gather) {
+      move_rows_kernel<uint32_t, true><<<blocks, kWarps * 32, 0, st>>>(s, idx, n, n_other, rv, d, err);
+    } else {
+      move_rows_kernel<uint32_t, false><<<blocks, kWarps * 32, 0, st>>>(s, idx, n, n_other, rv, d, err);
+    }
+  }
+  return cudaGetLastError();
+}
 
 int permute_chunks(int T) { return (T + kChunk - 1) / kChunk; }
 

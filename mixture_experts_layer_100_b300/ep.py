@@ -27,8 +27,9 @@ the single-GPU routed output yp in expert-major order; the gate-weighted
 combine then runs unchanged (moe_combine).
 
 Only index arithmetic lives here (torch integer ops, host or device); the
-exchange is torch.distributed's all_to_all_single. Row payloads are
-whatever the caller passes.
+exchange is torch.distributed's all_to_all_single, and the row reorders are
+the library's moe_gather_rows / moe_scatter_rows kernels on the device
+(device_row_moves), or whatever row-move functions the caller passes.
 """
 from __future__ import annotations
 
@@ -104,10 +105,13 @@ def ranks_reached(topk_idx: torch.Tensor, E: int, world: int) -> torch.Tensor:
     return onehot.sum(1)
 
 
-def dispatch(xp: torch.Tensor, offsets: torch.Tensor, counts: torch.Tensor, world: int, group=None, dist=None):
-    """All-to-all dispatch of a rank's permuted rows. Returns (rows in local
-    expert-major order, local_offsets, plan) where plan carries what combine
-    needs to send the outputs back."""
+def dispatch(xp: torch.Tensor, offsets: torch.Tensor, counts: torch.Tensor, world: int, gather_rows,
+             group=None, dist=None):
+    """All-to-all dispatch of a rank's permuted rows. gather_rows(src, idx)
+    returns src's rows in idx order (on the GPU: moe_gather_rows, see
+    device_row_moves). Returns (rows in local expert-major order,
+    local_offsets, plan) where plan carries what combine_back needs to send
+    the outputs back."""
     if dist is None:
         import torch.distributed as dist
     ss = send_splits(offsets, world)
@@ -118,17 +122,39 @@ def dispatch(xp: torch.Tensor, offsets: torch.Tensor, counts: torch.Tensor, worl
     recv = xp.new_empty((int(recv_splits.sum()),) + tuple(xp.shape[1:]))
     dist.all_to_all_single(recv, xp[: int(ss.sum())].contiguous(), output_split_sizes=recv_splits.tolist(),
                            input_split_sizes=ss.tolist(), group=group)
-    return recv[gather], local_offsets, {"send_splits": ss, "recv_splits": recv_splits, "gather": gather}
+    return gather_rows(recv, gather), local_offsets, {"send_splits": ss, "recv_splits": recv_splits,
+                                                      "gather": gather}
 
 
-def combine_back(y_local: torch.Tensor, plan, group=None, dist=None) -> torch.Tensor:
+def combine_back(y_local: torch.Tensor, plan, scatter_rows, group=None, dist=None) -> torch.Tensor:
     """Returns the expert outputs of this rank's own rows, in its
-    expert-major order (the yp of the single-GPU layer)."""
+    expert-major order (the yp of the single-GPU layer). scatter_rows(src,
+    idx, n_dst) returns dst with dst[idx[i]] = src[i]."""
     if dist is None:
         import torch.distributed as dist
-    y_recv = torch.empty_like(y_local)
-    y_recv[plan["gather"]] = y_local
+    y_recv = scatter_rows(y_local, plan["gather"], y_local.shape[0])
     out = y_local.new_empty((int(plan["send_splits"].sum()),) + tuple(y_local.shape[1:]))
     dist.all_to_all_single(out, y_recv, output_split_sizes=plan["send_splits"].tolist(),
                            input_split_sizes=plan["recv_splits"].tolist(), group=group)
     return out
+
+
+def device_row_moves(ws):
+    """(gather_rows, scatter_rows) for device tensors, run by the library's
+    moe_gather_rows / moe_scatter_rows kernels; ws is a workspace whose error
+    word they report bad indices in."""
+    from . import binding as B
+
+    def gather_rows(src, idx):
+        idx32 = idx.to(torch.int32).contiguous()
+        dst = src.new_empty((idx32.numel(),) + tuple(src.shape[1:]))
+        B.moe_gather_rows(src.contiguous(), idx32, dst, ws)
+        return dst
+
+    def scatter_rows(src, idx, n_dst):
+        idx32 = idx.to(torch.int32).contiguous()
+        dst = src.new_empty((n_dst,) + tuple(src.shape[1:]))
+        B.moe_scatter_rows(src.contiguous(), idx32, dst, ws)
+        return dst
+
+    return gather_rows, scatter_rows

@@ -1,4 +1,5 @@
-"""Expert parallelism on CPU ranks (gloo): each rank routes its own tokens,
+"""Expert parallelism on CPU ranks (gloo; the row reorders are plain torch
+indexing here, the library's kernels on GPUs): each rank routes its own tokens,
 sends its permuted rows to the ranks that hold their experts, runs its local
 experts on what it receives, and gets its rows' outputs back; combined with
 the gates, every rank's layer output must equal the single-process oracle's
@@ -39,6 +40,12 @@ def _tokens(rank):
     return np.random.default_rng(100 + rank).standard_normal((40 + 7 * rank, D))
 
 
+def _scatter_rows(src, idx, n_dst):
+    dst = src.new_empty((n_dst,) + tuple(src.shape[1:]))
+    dst[idx] = src
+    return dst
+
+
 def _worker(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -52,7 +59,8 @@ def _worker(rank, world, port, out):
         offsets = om.exclusive_offsets(counts)
         st, sp = om.permutation(idx, E)
         xp = torch.from_numpy(x[st])
-        rows, local_off, plan = ep.dispatch(xp, torch.from_numpy(offsets), torch.from_numpy(counts), world)
+        rows, local_off, plan = ep.dispatch(xp, torch.from_numpy(offsets), torch.from_numpy(counts), world,
+                                            gather_rows=lambda src, idx: src[idx])
         per = E // world
         y_local = torch.empty_like(rows)
         lo = local_off.numpy()
@@ -61,7 +69,7 @@ def _worker(rank, world, port, out):
             if lo[el + 1] > lo[el]:
                 y_local[lo[el]:lo[el + 1]] = torch.from_numpy(
                     om.swiglu_ffn(rows[lo[el]:lo[el + 1]].numpy(), w["w13"][e], w["w2"][e]))
-        yp = ep.combine_back(y_local, plan).numpy()
+        yp = ep.combine_back(y_local, plan, scatter_rows=_scatter_rows).numpy()
         res = om.shared_output(x, w["ws13"], w["ws2"])
         for k in range(K):
             res += gate[:, k:k + 1].astype(np.float64) * yp[sp[:, k]]
