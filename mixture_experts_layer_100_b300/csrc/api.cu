@@ -246,11 +246,16 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
     int32_t* slot_pos = at<int32_t>(ws, Lw.slot_pos);
     void* xp = at<void>(ws, Lw.xp);
     void* yp = at<void>(ws, Lw.yp);
+    // padded layout (zero_padded): experts start at multiples of 128, zero rows between
+    const bool padded = zero_padded(c);
+    const int rows = expert_rows(c);
     MOE_TRY(permute_stage(c, topk_idx, counts, offsets, at<int32_t>(ws, Lw.sorted_tok), slot_pos, x, xp,
                           f8 ? at<float>(ws, Lw.xp_scale) : nullptr, nullptr, nullptr, ws, st,
-                          scat ? topk_gate : nullptr, scat ? at<float>(ws, Lw.gate_p) : nullptr, f32));
+                          scat ? topk_gate : nullptr, scat ? at<float>(ws, Lw.gate_p) : nullptr, f32,
+                          padded ? 128 : 1));
     MOE_TRY(stage_mark(3, st));
-    MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, false, ws, st));
+    MOE_TRY(gemm1_stage(c, xp, f8 ? at<float>(ws, Lw.xp_scale) : nullptr, offsets, x, w, true, false, ws, st,
+                        rows));
     MOE_TRY(stage_mark(4, st));
     if (scat) {
       MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
@@ -258,7 +263,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
       MOE_TRY(stage_mark(5, st));
       if (!f32) MOE_TRY(acc_round_stage(c, acc, out, st));
     } else {
-      MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st));
+      MOE_TRY(gemm2_routed_stage(c, offsets, w, yp, ws, st, rows, padded ? counts : nullptr));
       MOE_TRY(stage_mark(5, st));
       if (side != nullptr) MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
       MOE_TRY(gemm2_combine_stage(c, yp, slot_pos, topk_gate, w, out, ws, st));

@@ -26,6 +26,7 @@ struct Sched {
   const int* tp;    // [groups0 + 1] first tile of each group (shared memory)
   const int* mt;    // [groups0] m-tiles of each group
   const int* off;   // [groups0 + 1] row offsets
+  const int* end = nullptr;  // [groups0] last row + 1 of each group's stored rows (NULL: off[g + 1])
   int groups0, tiles0, total;
   int n_tiles0, n_tiles1, mt1, rows1;
   int bm = kBM;                // rows per tile
@@ -52,7 +53,7 @@ struct Sched {
       t.group = lo;
       raster(L - tp[lo], mt[lo], n_tiles0, t.m, t.n);
       t.row0 = off[lo] + t.m * bm;
-      t.row_end = off[lo + 1];
+      t.row_end = end != nullptr ? end[lo] : off[lo + 1];
     } else {
       t.seg = 1;
       t.group = 0;

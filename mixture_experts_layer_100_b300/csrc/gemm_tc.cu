@@ -10,7 +10,7 @@ namespace {
 
 constexpr int kBK = 64;           // bf16 elements per 128-byte swizzle row
 constexpr int kUK = 16;           // K per tcgen05.mma (kind::f16)
-constexpr int kAuxBytes = 8192;
+constexpr int kAuxBytes = 12288;
 constexpr int kRingBytes = 196608;
 
 // A tile is MH 128-row halves x BN columns: the halves share each staged B
@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(Cfg<BN, MH, SPLIT>::kThreads, 1)
   int* s_tp = reinterpret_cast<int*>(aux + 256);
   int* s_mt = s_tp + (kMaxGroups + 1);
   int* s_off = s_mt + kMaxGroups;
+  int* s_end = s_off + (kMaxGroups + 1);  // stored rows' end per group (counts0)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(Cfg<BN, MH, SPLIT>::kThreads, 1)
     for (int g = beg; g < end; ++g) {
       const int o0 = p.offsets0[g], o1 = p.offsets0[g + 1];
       s_off[g] = o0;
+      if (p.counts0 != nullptr) s_end[g] = o0 + min(p.counts0[g], o1 - o0);
       const int mt = (o1 - o0 + BMT - 1) / BMT;
       s_mt[g] = mt;
       sum += mt;
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(Cfg<BN, MH, SPLIT>::kThreads, 1)
   sch.tp = s_tp;
   sch.mt = s_mt;
   sch.off = s_off;
+  sch.end = p.counts0 != nullptr ? s_end : nullptr;
   sch.groups0 = p.groups0;
   sch.tiles0 = s_tp[p.groups0];
   sch.n_tiles0 = p.n_tiles0;

@@ -39,6 +39,9 @@ enum class Epi : int {
 struct TcGemmParams {
   int groups0;          // segment 0 groups (0: no segment 0)
   const int* offsets0;  // [groups0 + 1] device row offsets of segment 0
+  // [groups0] or NULL: rows of each group that are written (the padded
+  // layout's groups end with zero rows that are multiplied but not stored)
+  const int* counts0;
   int rows1;            // rows of segment 1 (0: no segment 1)
   int n_tiles0, n_tiles1;
   int k_blocks0, k_blocks1;  // K / 64 per segment

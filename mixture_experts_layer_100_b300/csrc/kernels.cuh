@@ -19,12 +19,16 @@ cudaError_t launch_seq_balance(const float* scores, const int* topk_idx, int T, 
 int permute_chunks(int T);
 cudaError_t launch_permute_rank(const int* topk_idx, int T, int K, int E, int* local_rank, int* chunk_hist, int* err,
                                 cudaStream_t st);
+// pad > 1: every expert's block of rows starts at a multiple of pad (its
+// rows followed by up to pad - 1 unused rows), which the scatter fills with
+// zeros (given offsets and counts).
 cudaError_t launch_permute_scan(const int* counts, const int* chunk_hist, int T, int E, int* chunk_base, int* offsets,
-                                int* err, cudaStream_t st);
+                                int* err, cudaStream_t st, int pad = 1);
 cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, const int* chunk_base, int T, int K,
                                    int E, const void* x, size_t row_bytes, int* sorted_tok, int* slot_pos, void* xp,
                                    int num_sms, cudaStream_t st, const float* gate_in = nullptr,
-                                   float* gate_p = nullptr);
+                                   float* gate_p = nullptr, int pad = 1, const int* offsets = nullptr,
+                                   const int* counts = nullptr);
 cudaError_t launch_permute_scatter_e4m3(const int* topk_idx, const int* local_rank, const int* chunk_base, int T,
                                         int K, int E, const __nv_bfloat16* x, int d, int* sorted_tok, int* slot_pos,
                                         uint8_t* xp, float* xp_scale, uint8_t* xq, float* xq_scale, float* tok_scale,

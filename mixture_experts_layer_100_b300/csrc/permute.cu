@@ -13,6 +13,10 @@
 //   scatter one warp per token: position = base[e][chunk] + rank; writes
 //           slot_pos / sorted_tok and copies the token row to its K places
 //           with 16-byte vector accesses (optionally quantising it to e4m3).
+// Optionally (pad > 1) every expert's rows start at a multiple of pad and
+// the scatter zeroes the unused rows after them, so that the expert GEMMs'
+// last tile of each expert multiplies zeros instead of the next expert's
+// rows (the same instructions; zero operands draw less power).
 #include "kernels.cuh"
 
 namespace moe {
@@ -59,12 +63,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 __global__ void __launch_bounds__(kWarps * 32)
     permute_scan_kernel(const int* __restrict__ counts, const int* __restrict__ chunk_hist, int E, int nchunks,
-                        int* __restrict__ chunk_base, int* __restrict__ offsets, int* err) {
+                        int* __restrict__ chunk_base, int* __restrict__ offsets, int* err, int pad) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kWarps + warp;
   if (e >= E) return;
-  int start = 0;
-  for (int j = lane; j < e; j += 32) start += counts[j];
+  int start = 0;  // rows of the experts before e, each rounded up to pad
+  for (int j = lane; j < e; j += 32) start += (counts[j] + pad - 1) / pad * pad;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) start += __shfl_xor_sync(0xffffffffu, start, o);
   const int* h = chunk_hist + (size_t)e * nchunks;
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   if (lane == 0) {
     if (carry - start != counts[e]) set_error(err, kDevCountMismatch);
     offsets[e] = start;
-    if (e == E - 1) offsets[E] = start + counts[e];
+    if (e == E - 1) offsets[E] = start + (counts[e] + pad - 1) / pad * pad;
   }
 }
 
@@ -95,8 +99,22 @@ __global__ void __launch_bounds__(kWarps * 32)
                            const int* __restrict__ chunk_base, int T, int K, int E, int nchunks,
                            const VecT* __restrict__ x, int row_vecs, int* __restrict__ sorted_tok,
                            int* __restrict__ slot_pos, VecT* __restrict__ xp, const float* __restrict__ gate_in,
-                           float* __restrict__ gate_p) {
+                           float* __restrict__ gate_p, int pad, const int* __restrict__ offsets,
+                           const int* __restrict__ counts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (pad > 1) {
+    // the unused rows of the padded layout: item (e, j) is row
+    // offsets[e] + counts[e] + j when that is before offsets[e + 1]
+    const VecT zero = {};
+    for (int i = blockIdx.x * kWarps + warp; i < E * pad; i += gridDim.x * kWarps) {
+      const int e = i / pad;
+      const int row = offsets[e] + counts[e] + i % pad;
+      if (row < offsets[e + 1]) {
+        VecT* dst = xp + (size_t)row * row_vecs;
+        for (int v = lane; v < row_vecs; v += 32) dst[v] = zero;
+      }
+    }
+  }
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     int pos = 0;
     if (lane < K) {
@@ -321,26 +339,28 @@ cudaError_t launch_permute_rank(const int* topk_idx, int T, int K, int E, int* l
 }
 
 cudaError_t launch_permute_scan(const int* counts, const int* chunk_hist, int T, int E, int* chunk_base, int* offsets,
-                                int* err, cudaStream_t st) {
+                                int* err, cudaStream_t st, int pad) {
   const int nchunks = permute_chunks(T);
   permute_scan_kernel<<<(E + kWarps - 1) / kWarps, kWarps * 32, 0, st>>>(counts, chunk_hist, E, nchunks, chunk_base,
-                                                                         offsets, err);
+                                                                         offsets, err, pad);
   return cudaGetLastError();
 }
 
 cudaError_t launch_permute_scatter(const int* topk_idx, const int* local_rank, const int* chunk_base, int T, int K,
                                    int E, const void* x, size_t row_bytes, int* sorted_tok, int* slot_pos, void* xp,
-                                   int num_sms, cudaStream_t st, const float* gate_in, float* gate_p) {
+                                   int num_sms, cudaStream_t st, const float* gate_in, float* gate_p, int pad,
+                                   const int* offsets, const int* counts) {
   const int nchunks = permute_chunks(T);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 8));
+  if (pad > 1 && (offsets == nullptr || counts == nullptr)) return cudaErrorInvalidValue;
   if (row_bytes % 16 == 0) {
     permute_scatter_kernel<uint4><<<blocks, kWarps * 32, 0, st>>>(
         topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint4*>(x), (int)(row_bytes / 16),
-        sorted_tok, slot_pos, static_cast<uint4*>(xp), gate_in, gate_p);
+        sorted_tok, slot_pos, static_cast<uint4*>(xp), gate_in, gate_p, pad, offsets, counts);
   } else {
     permute_scatter_kernel<uint32_t><<<blocks, kWarps * 32, 0, st>>>(
         topk_idx, local_rank, chunk_base, T, K, E, nchunks, static_cast<const uint32_t*>(x), (int)(row_bytes / 4),
-        sorted_tok, slot_pos, static_cast<uint32_t*>(xp), gate_in, gate_p);
+        sorted_tok, slot_pos, static_cast<uint32_t*>(xp), gate_in, gate_p, pad, offsets, counts);
   }
   return cudaGetLastError();
 }

@@ -31,21 +31,22 @@ Layout layout(const moe_config& c) {
   L.chunk_hist = take(E * nch * 4);
   L.chunk_base = take(E * nch * 4);
   L.offsets = take((E + 1) * 4);
-  L.sorted_tok = take(TK * 4);
+  const size_t ER = (size_t)expert_rows(c);  // T * K, plus the padding rows of the padded layout
+  L.sorted_tok = take(ER * 4);                 // indexed by row position
   L.slot_pos = take(TK * 4);
   const size_t pairs = c.act == MOE_F32 ? 2 : 1;  // fp32 GEMM operands are stored as tf32 pairs
-  L.xp = take(TK * d * ex * pairs);
+  L.xp = take(ER * d * ex * pairs);
   L.xp_scale = take(f8 ? (d / 128) * TK * 4 : 0);
   L.xq = take(f8 ? T * d : 0);
   L.xq_scale = take(f8 ? (d / 128) * T * 4 : 0);
   L.tok_scale = take(f8 ? (d / 128) * T * 4 : 0);
-  L.h = take(TK * I * ex * pairs);
+  L.h = take(ER * I * ex * pairs);
   L.h_scale = take(f8 ? (I / 128) * TK * 4 : 0);
   L.hs = take(T * S * I * ex * pairs);
   L.hs_scale = take(f8 ? (S * I / 128) * T * 4 : 0);
   const bool scat = scatter_combine(c);
-  L.yp = take(scat ? 0 : TK * d * ea);
-  L.gate_p = take(scat ? TK * 4 : 0);
+  L.yp = take(scat ? 0 : ER * d * ea);
+  L.gate_p = take(scat ? ER * 4 : 0);
   L.acc = take(scat && c.act == MOE_BF16 ? T * d * 4 : 0);  // fp32 layers add into out itself
   const bool f32 = c.act == MOE_F32;
   L.xs = take(f32 ? T * 2 * d * 4 : 0);
@@ -247,7 +248,7 @@ moe_status route_stage(const moe_config& c, const void* x, const void* w_router,
 moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int32_t* counts, int32_t* offsets,
                          int32_t* sorted_tok, int32_t* slot_pos, const void* x, void* xp, float* xp_scale,
                          uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st, const float* gate,
-                         float* gate_p, bool pairs) {
+                         float* gate_p, bool pairs, int pad) {
   const Layout Lw = layout(c);
   if (c.T == 0) {
     MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), st));
@@ -258,7 +259,7 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
   int* chunk_hist = at<int>(ws, Lw.chunk_hist);
   int* chunk_base = at<int>(ws, Lw.chunk_base);
   MOE_CUDA(launch_permute_rank(topk_idx, c.T, c.K, c.E, local_rank, chunk_hist, err, st));
-  MOE_CUDA(launch_permute_scan(counts, chunk_hist, c.T, c.E, chunk_base, offsets, err, st));
+  MOE_CUDA(launch_permute_scan(counts, chunk_hist, c.T, c.E, chunk_base, offsets, err, st, pad));
   if (is_f8(c.expert)) {
     MOE_CUDA(launch_permute_scatter_e4m3(topk_idx, local_rank, chunk_base, c.T, c.K, c.E,
                                          static_cast<const __nv_bfloat16*>(x), c.d, sorted_tok, slot_pos,
@@ -268,7 +269,7 @@ moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int
   } else {
     MOE_CUDA(launch_permute_scatter(topk_idx, local_rank, chunk_base, c.T, c.K, c.E, x,
                                     (size_t)c.d * elem_bytes(c.act) * (pairs ? 2 : 1), sorted_tok, slot_pos, xp,
-                                    num_sms(), st, gate, gate_p));
+                                    num_sms(), st, gate, gate_p, pad, offsets, counts));
   }
   return MOE_OK;
 }
@@ -381,9 +382,10 @@ static moe_status fp8_gemm2(const moe_config& c, const int32_t* offsets, const m
 
 // GEMM1 (SwiGLU) of the routed experts over xp and/or the shared experts over x.
 moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
-                       const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st) {
+                       const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st,
+                       int rows) {
   const Layout Lw = layout(c);
-  const int TK = c.T * c.K;
+  const int TK = rows < 0 ? c.T * c.K : rows;
   if (is_f8(c.expert)) {
     return fp8_gemm1(c, xp, xp_scale, offsets, at<uint8_t>(ws, Lw.xq), at<float>(ws, Lw.xq_scale), w, routed,
                      shared, ws, st);
@@ -478,9 +480,9 @@ static moe_status down_maps(const moe_config& c, TcGemmLaunch& L, bool seg1, con
 
 // GEMM2 of the routed experts: yp = h W2^T (not gate-scaled).
 moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, void* yp, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, int rows, const int32_t* counts) {
   const Layout Lw = layout(c);
-  const int TK = c.T * c.K;
+  const int TK = rows < 0 ? c.T * c.K : rows;
   if (is_f8(c.expert)) return fp8_gemm2(c, offsets, w, yp, false, nullptr, nullptr, ws, st);
   TcGemmLaunch L{};
   L.epi = c.act == MOE_F32 ? Epi::kStoreF32 : Epi::kStore;
@@ -489,6 +491,7 @@ moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const
   MOE_TRY(down_maps(c, L, false, at<void>(ws, Lw.h), c.I, TK, w->w2, f32_weights(c, ws).w2, c.E));
   L.p.groups0 = c.E;
   L.p.offsets0 = offsets;
+  L.p.counts0 = counts;
   L.p.n_tiles0 = c.d / L.bn;
   L.p.out0 = yp;
   L.p.ldo0 = c.d;

@@ -40,6 +40,20 @@ inline bool scatter_combine(const moe_config& c) {
   return c.combine == MOE_COMBINE_SCATTER_ADD && c.act == c.expert;
 }
 
+// moe_layer_forward's expert-row layout: with bf16 expert GEMMs, the gather
+// combine and at least 128 rows per expert on average, every expert's rows
+// start at a multiple of 128 and the (at most 127) rows after them are zero,
+// so the last tile of each expert multiplies zeros, not the next expert's
+// rows (same results, less power under the cap). Other layers, and the
+// separate entry points, keep the rows contiguous.
+inline bool zero_padded(const moe_config& c) {
+  const long long tk = (long long)c.T * c.K;
+  return c.act == MOE_BF16 && c.expert == MOE_BF16 && !scatter_combine(c) && tk >= 128LL * c.E &&
+         tk + 127LL * c.E <= 0x7fffffffLL;
+}
+// Rows of the layer's permuted buffers (xp, h, yp).
+inline int expert_rows(const moe_config& c) { return c.T * c.K + (zero_padded(c) ? 127 * c.E : 0); }
+
 // ------------------------------------------------------------ workspace
 struct Layout {
   size_t err, scores, local_rank, chunk_hist, chunk_base, offsets, sorted_tok, slot_pos;
@@ -81,11 +95,16 @@ moe_status route_stage(const moe_config& c, const void* x, const void* w_router,
 moe_status permute_stage(const moe_config& c, const int32_t* topk_idx, const int32_t* counts, int32_t* offsets,
                          int32_t* sorted_tok, int32_t* slot_pos, const void* x, void* xp, float* xp_scale,
                          uint8_t* xq, float* xq_scale, void* ws, cudaStream_t st, const float* gate = nullptr,
-                         float* gate_p = nullptr, bool pairs = false);
+                         float* gate_p = nullptr, bool pairs = false, int pad = 1);
+// rows: rows of xp and of the workspace h (T * K, or expert_rows(c) for the
+// padded layout).
 moe_status gemm1_stage(const moe_config& c, const void* xp, const float* xp_scale, const int32_t* offsets,
-                       const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st);
+                       const void* x, const moe_weights* w, bool routed, bool shared, void* ws, cudaStream_t st,
+                       int rows = -1);
+// counts (padded layout): the down projection writes only each expert's own
+// rows, not the zero rows after them.
 moe_status gemm2_routed_stage(const moe_config& c, const int32_t* offsets, const moe_weights* w, void* yp, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, int rows = -1, const int32_t* counts = nullptr);
 // Scatter-add combine: the shared experts' down projection writes the fp32
 // accumulator (zeros when S = 0); the routed down projection adds gate * row
 // into it; the accumulator is rounded to bf16 out.

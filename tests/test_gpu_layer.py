@@ -34,6 +34,8 @@ SMALL = {
     "t150_d256_e64_k16": dict(T=150, d=256, E=64, G=4, K=16, M=2, I=128, S=1),
     "t90_d256_e64_k32": dict(T=90, d=256, E=64, G=2, K=32, M=1, I=128, S=1),
     "t257_d256_e32_k1": dict(T=257, d=256, E=32, G=4, K=1, M=1, I=128, S=1),   # top-1 routing, one group
+    # T * K >= 128 E: the bf16 layer uses the zero-padded expert layout
+    "t520_d256_e8_padded": dict(T=520, d=256, E=8, G=4, K=2, M=2, I=128, S=1),
 }
 
 
@@ -147,11 +149,13 @@ def test_empty_batch_is_a_no_op():
     assert counts.sum().item() == 0 and b.abs().sum().item() == 0
 
 
-def test_entry_points_compose_to_the_layer():
+@pytest.mark.parametrize("name", ["t515_d384_e32_i384_s2", "t520_d256_e8_padded"])
+def test_entry_points_compose_to_the_layer(name):
     """route -> permute -> grouped_ffn -> combine -> bias_update gives the
-    same bits as moe_layer_forward."""
+    same bits as moe_layer_forward (for t520 the layer runs its experts on the
+    zero-padded row layout, the entry points on contiguous rows)."""
     from mixture_experts_layer_100_b300 import binding as B
-    p = small_preset("t515_d384_e32_i384_s2")
+    p = small_preset(name)
     w = synth.make_weights(p)
     x = synth.make_x(p, w.w_router).to(DEV)
     b0 = synth.make_bias(p).to(DEV)
