@@ -74,9 +74,14 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E4M3_UE8M0 = 3 } moe
 
 /* How moe_layer_forward combines the routed experts' rows [resmic-moe]:
  * MOE_COMBINE_GATHER: the routed down projection writes each expert row once
- *   (unscaled, [T*K, d] in the workspace); a per-token pass sums the K gated
- *   rows of each token in a fixed order and the shared experts' down
- *   projection adds that sum in its epilogue. Deterministic.
+ *   (unscaled, in the workspace); a per-token pass sums the K gated rows of
+ *   each token in a fixed order and the shared experts' down projection adds
+ *   that sum in its epilogue. Deterministic. With bf16 expert GEMMs and
+ *   T*K >= 128*E the layer keeps its permuted rows in a padded layout inside
+ *   the workspace (each expert's rows start at a multiple of 128, followed by
+ *   zero rows up to it) so that the expert GEMMs' last tile of each expert
+ *   multiplies zeros; the results are the same bits as with contiguous rows,
+ *   and moe_workspace_size accounts for the 127*E extra rows.
  * MOE_COMBINE_SCATTER_ADD: the shared experts' down projection writes an fp32
  *   [T, d] accumulator, the routed down projection's epilogue adds gate * row
  *   into it with fp32 reductions (red.global.add), and one pass rounds it to
