@@ -17,6 +17,7 @@ workload and prints the same kind of line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -85,7 +86,11 @@ def peaks():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks, power and throttle reasons every 50 ms. The sampler
+    is started before the timed region and waits (up to 3 s) for its first
+    sample; mark(start/end) bracket the timed region on the host clock, and
+    summary() keeps the samples taken inside it (all samples if none)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -93,6 +98,7 @@ class ClockSampler:
         self.enabled = enabled
         self.idx = device_index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         if not self.enabled:
@@ -101,10 +107,20 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.tmp, stderr=subprocess.DEVNULL)
         except FileNotFoundError:
             self.proc = None
+            return self
+        deadline = time.time() + 3.0
+        while time.time() < deadline and os.path.getsize(self.tmp.name) == 0:
+            time.sleep(0.02)
         return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -114,34 +130,47 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    @staticmethod
+    def parse(lines, t0=None, t1=None):
+        """Samples of nvidia-smi csv lines (FIELDS order) -> summary dict;
+        only those stamped within [t0, t1] when any are."""
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
+        for line in lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm, mx = float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None  # unknown stamp format: the sample counts only among all samples
+            try:
+                pw = float(f[4])
+            except ValueError:
+                pw = None
+            rows.append((ts, sm, mx, pw, [n for n, v in zip(names, f[6:10]) if v.lower().startswith("active")]))
+        if not rows:
+            return None
+        inside = [r for r in rows if None not in (t0, t1, r[0]) and t0 <= r[0] <= t1]
+        use = inside or rows
+        pws = [r[3] for r in use if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted({n for r in use for n in r[4]}), "samples": len(use),
+                "samples_in_timed_region": len(inside),
+                "power_w_median": statistics.median(pws) if pws else None}
+
     def summary(self):
         if self.proc is None:
             return None
         self.tmp.flush()
         self.tmp.seek(0)
-        sm, mx, pw, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.tmp.read().strip().splitlines():
-            f = [v.strip() for v in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            try:
-                pw.append(float(f[3]))
-            except ValueError:
-                pass
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        lines = self.tmp.read().strip().splitlines()
         os.unlink(self.tmp.name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None}
+        return self.parse(lines, self.t0, self.t1)
 
 
 # ---------------------------------------------------------------- helpers
@@ -732,12 +761,14 @@ def run_ours(a, p):
     sampler = ClockSampler(local, enabled=not a.no_clocks and rank == 0)
     with sampler:
         torch.cuda.synchronize()
+        sampler.mark_start()
         t_start.record()
         for i in range(K):
             B.moe_set_stage_events(ev[i])
             step()
         t_end.record()
         torch.cuda.synchronize()
+        sampler.mark_end()
     B.moe_set_stage_events(None)
     if pg:
         pg.barrier()

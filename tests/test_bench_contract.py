@@ -45,3 +45,22 @@ def test_reference_arm_other_ranks_print_nothing():
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_clock_samples_are_taken_from_the_timed_region():
+    """The clocks summary keeps the nvidia-smi samples stamped inside the
+    timed region (all samples when none are) and reports throttle reasons."""
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = ["2026/12/03 10:00:00.100, 0, 1300, 2032, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
+             "2026/12/03 10:00:00.150, 0, 1350, 2032, 950.5, 0x4, Not Active, Not Active, Not Active, Active",
+             "2026/12/03 10:00:01.150, 0, 1900, 2032, 150.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbled line"]
+    t0, t1 = datetime.datetime(2026, 12, 3, 10, 0, 0), datetime.datetime(2026, 12, 3, 10, 0, 1)
+    s = bench.ClockSampler.parse(lines, t0, t1)
+    assert s["samples_in_timed_region"] == 2 and s["sm_mhz"] == 1325.0 and s["power_w_median"] == 925.5
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2032.0
+    s = bench.ClockSampler.parse(lines)
+    assert s["samples"] == 3 and s["samples_in_timed_region"] == 0 and s["sm_mhz"] == 1350.0
+    assert bench.ClockSampler.parse(["garbled"]) is None
