@@ -465,6 +465,10 @@ def run_standalone_memory_stages(B, cfg, p, x, w_router, bias, ws, f8, hbm, reps
     return out
 
 
+def layer_graphs_on():
+    return os.environ.get("MOE_LAYER_GRAPHS", "1")[:1] != "0"
+
+
 def run_graph_replay(step, p, K, dev, world):
     """One layer step captured into a CUDA graph (after the eager steps above
     created the library's side stream) and replayed K times, timed with CUDA
@@ -877,6 +881,10 @@ def run_ours(a, p):
             "other_workloads": extra,
             "e2e": e2e,
             "gpu_launches": kernels_per_step(p) * K,
+            "launch": {"layer_graphs": layer_graphs_on(),
+                       "note": "moe_layer_forward replays a CUDA graph of its kernels, captured by the library at "
+                               "the second call with the same arguments (MOE_LAYER_GRAPHS=0 launches them one "
+                               "by one); gpu_launches counts the kernels either way"},
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

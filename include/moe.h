@@ -258,6 +258,27 @@ moe_status moe_gather_rows(const void* src, int n_src, const int32_t* idx, int n
 moe_status moe_scatter_rows(const void* src, const int32_t* idx, int n, size_t row_bytes, void* dst, int n_dst,
                             void* ws, moe_stream_t stream);
 
+/* CUDA-graph replay of moe_layer_forward (on by default; the environment
+ * variable MOE_LAYER_GRAPHS=0 starts the process with it off). When on, the
+ * second call with the same configuration, pointers, gamma and stage-event
+ * setting (moe_set_stage_events on or off) on the same CUDA context is
+ * captured into a graph, and that call and every later one with the same
+ * arguments replay it with one cudaGraphLaunch on the caller's stream: the
+ * same kernels with the same arguments, so the same results, without the
+ * per-kernel launch gaps. The events given to moe_set_stage_events are
+ * re-targeted on each replay. Calls on a stream that is itself being captured
+ * run the kernels directly (they become part of the caller's graph). Up to 16
+ * argument sets are kept per process, the least recently used one replaced
+ * by a new one. A graph holds the pointers it was captured with: a buffer
+ * freed and reallocated at the same address with the same configuration is
+ * used as the new buffer, as with any cached launch.
+ * enable: 1 on, 0 off (the kept graphs stay, unused). MOE_ERR_INVALID_ARG
+ * for other values. */
+moe_status moe_set_layer_graphs(int enable);
+/* Number of argument sets that moe_layer_forward currently replays from a
+ * graph (written to *n). */
+moe_status moe_layer_graphs_kept(int* n);
+
 /* Bytes of the fixed device array that moe_permute_static uses as scratch. */
 #define MOE_PERMUTE_STATIC_SCRATCH_BYTES (4u << 20)
 

@@ -69,6 +69,8 @@ _SIGS = {
     "moe_scatter_rows": [_P, _P, ctypes.c_int, ctypes.c_size_t, _P, ctypes.c_int, _P, _P],
     "moe_set_stage_events": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int],
     "moe_selftest_timeout": [_P, _P],
+    "moe_set_layer_graphs": [ctypes.c_int],
+    "moe_layer_graphs_kept": [ctypes.POINTER(ctypes.c_int)],
     "moe_device_error": [_P, _P, ctypes.POINTER(ctypes.c_int)],
     "moe_status_string": [ctypes.c_int],
 }
@@ -212,6 +214,17 @@ def moe_set_stage_events(events) -> None:
         return
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("moe_set_stage_events", lib.moe_set_stage_events(arr, len(events)))
+
+
+def moe_set_layer_graphs(enable: bool) -> None:
+    """Switch the CUDA-graph replay of moe_layer_forward on or off."""
+    _check("moe_set_layer_graphs", lib.moe_set_layer_graphs(1 if enable else 0))
+
+
+def moe_layer_graphs_kept() -> int:
+    n = ctypes.c_int(0)
+    _check("moe_layer_graphs_kept", lib.moe_layer_graphs_kept(ctypes.byref(n)))
+    return n.value
 
 
 def moe_selftest_timeout(ws, stream=None) -> None:

@@ -1,6 +1,8 @@
 // C ABI of the MoE layer library: argument checks and the launch sequence
 // of each entry point (see moe.h); the stages themselves are in stages.cu.
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "kernels.cuh"
 #include "moe.h"
@@ -82,9 +84,154 @@ moe_status side_stream(SideStream** out) {
 
 thread_local cudaEvent_t g_stage_events[8];
 thread_local bool g_stage_on = false;
+thread_local bool g_capturing = false;  // moe_layer_forward is being captured into a graph
 
 moe_status stage_mark(int i, cudaStream_t st) {
-  if (g_stage_on) MOE_CUDA(cudaEventRecord(g_stage_events[i], st));
+  if (!g_stage_on) return MOE_OK;
+  // inside a capture the record becomes a graph node (re-targeted at replay)
+  if (g_capturing) {
+    MOE_CUDA(cudaEventRecordWithFlags(g_stage_events[i], st, cudaEventRecordExternal));
+  } else {
+    MOE_CUDA(cudaEventRecord(g_stage_events[i], st));
+  }
+  return MOE_OK;
+}
+
+moe_status layer_forward_body(const moe_config& c, const void* x, const moe_weights* w, float* bias, float gamma,
+                              void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts, float* max_over_mean,
+                              void* ws, cudaStream_t st);
+
+// ---- CUDA-graph replay of moe_layer_forward. A call with the same
+// configuration, buffers, gamma and stage-event setting as an earlier one on
+// the same context replays the kernels captured at the second such call
+// (same kernels, same arguments, so the same bits) instead of launching them
+// one by one. Up to kMaxGraphs argument sets are kept; a new one replaces the
+// least recently used (its executable graph is freed once any replay in
+// flight has finished).
+constexpr int kMaxGraphs = 16;
+
+struct LayerKey {
+  void* ctx;
+  moe_config cfg;
+  moe_weights w;
+  const void* x;
+  float* bias;
+  uint32_t gamma_bits;
+  void* out;
+  int32_t* idx;
+  float* gate;
+  int32_t* counts;
+  float* mom;
+  void* ws;
+  int stage_on;
+};
+
+struct LayerGraph {
+  LayerKey key;
+  unsigned long long last_use = 0;
+  int calls = 0;
+  bool failed = false;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t stage_nodes[8] = {};
+};
+
+std::mutex g_graph_mu;
+std::vector<LayerGraph>* g_graphs = new std::vector<LayerGraph>();  // never freed: outlives static teardown
+unsigned long long g_graph_clock = 0;
+
+void release_graph(LayerGraph& g) {
+  if (g.exec != nullptr) cudaGraphExecDestroy(g.exec);  // deferred by CUDA while a launch is in flight
+  if (g.graph != nullptr) cudaGraphDestroy(g.graph);
+  g = LayerGraph();
+}
+int g_graphs_mode = -1;  // -1: from MOE_LAYER_GRAPHS (default on), 0 off, 1 on
+
+bool layer_graphs_on() {
+  if (g_graphs_mode < 0) {
+    const char* v = getenv("MOE_LAYER_GRAPHS");
+    g_graphs_mode = (v != nullptr && v[0] == '0') ? 0 : 1;
+  }
+  return g_graphs_mode == 1;
+}
+
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(p);
+  }
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// Stream the captures are recorded on (one per host thread and device).
+moe_status capture_stream(cudaStream_t* out) {
+  thread_local cudaStream_t cache[64] = {};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  if (cache[dev] == nullptr) MOE_CUDA(cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking));
+  *out = cache[dev];
+  return MOE_OK;
+}
+
+moe_status capture_layer(LayerGraph& g, const moe_config& c, const void* x, const moe_weights* w, float* bias,
+                         float gamma, void* out, int32_t* idx, float* gate, int32_t* counts, float* mom, void* ws) {
+  cudaStream_t cap = nullptr;
+  MOE_TRY(capture_stream(&cap));
+  MOE_CUDA(cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal));
+  g_capturing = true;
+  const moe_status s = layer_forward_body(c, x, w, bias, gamma, out, idx, gate, counts, mom, ws, cap);
+  g_capturing = false;
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cap, &graph);
+  if (s != MOE_OK || e != cudaSuccess || graph == nullptr) {
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    (void)cudaGetLastError();
+    return s != MOE_OK ? s : MOE_ERR_CUDA;
+  }
+  if (cudaGraphInstantiate(&g.exec, graph, 0) != cudaSuccess) {
+    g.exec = nullptr;
+    cudaGraphDestroy(graph);
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  g.graph = graph;
+  if (g.key.stage_on) {
+    // the stage-event record nodes, to point them at each call's events
+    size_t n = 0;
+    MOE_CUDA(cudaGraphGetNodes(graph, nullptr, &n));
+    std::vector<cudaGraphNode_t> nodes(n);
+    MOE_CUDA(cudaGraphGetNodes(graph, nodes.data(), &n));
+    for (cudaGraphNode_t node : nodes) {
+      cudaGraphNodeType t;
+      MOE_CUDA(cudaGraphNodeGetType(node, &t));
+      if (t != cudaGraphNodeTypeEventRecord) continue;
+      cudaEvent_t ev = nullptr;
+      MOE_CUDA(cudaGraphEventRecordNodeGetEvent(node, &ev));
+      for (int i = 0; i < 8; ++i)
+        if (ev == g_stage_events[i] && g.stage_nodes[i] == nullptr) {
+          g.stage_nodes[i] = node;
+          break;
+        }
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status replay_layer(LayerGraph& g, cudaStream_t st) {
+  if (g.key.stage_on) {
+    for (int i = 0; i < 8; ++i)
+      if (g.stage_nodes[i] != nullptr)
+        MOE_CUDA(cudaGraphExecEventRecordNodeSetEvent(g.exec, g.stage_nodes[i], g_stage_events[i]));
+  }
+  MOE_CUDA(cudaGraphLaunch(g.exec, st));
   return MOE_OK;
 }
 
@@ -199,6 +346,87 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
     return MOE_ERR_INVALID_ARG;
   if (c.T > 0 && (!ok_ptr(x) || !ok_ptr(out) || !ok_ptr(w->w_router))) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (c.T > 0 && layer_graphs_on()) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    MOE_CUDA(cudaStreamIsCapturing(st, &cs));
+    if (cs == cudaStreamCaptureStatusNone) {  // (a caller's own capture records the kernels themselves)
+      LayerKey k;
+      memset(&k, 0, sizeof(k));
+      k.ctx = current_context();
+      k.cfg = c;
+      k.w = *w;
+      k.x = x;
+      k.bias = bias;
+      memcpy(&k.gamma_bits, &gamma, sizeof(float));
+      k.out = out;
+      k.idx = topk_idx;
+      k.gate = topk_gate;
+      k.counts = counts;
+      k.mom = max_over_mean;
+      k.ws = ws;
+      k.stage_on = g_stage_on ? 1 : 0;
+      std::lock_guard<std::mutex> lock(g_graph_mu);
+      LayerGraph* g = nullptr;
+      for (LayerGraph& e : *g_graphs)
+        if (memcmp(&e.key, &k, sizeof(k)) == 0) g = &e;
+      if (g == nullptr && k.ctx != nullptr) {
+        if ((int)g_graphs->size() < kMaxGraphs) {
+          g_graphs->reserve(kMaxGraphs);  // entries never move
+          g_graphs->emplace_back();
+          g = &g_graphs->back();
+        } else {
+          g = &(*g_graphs)[0];
+          for (LayerGraph& e : *g_graphs)
+            if (e.last_use < g->last_use) g = &e;
+          release_graph(*g);
+        }
+        g->key = k;
+      }
+      if (g != nullptr) g->last_use = ++g_graph_clock;
+      if (g != nullptr && !g->failed) {
+        if (g->exec == nullptr && ++g->calls >= 2) {
+          // first repeat of this argument set: capture it (the first call ran
+          // eagerly and set up the side stream, smem limits and tensor-map
+          // encoder outside any capture)
+          if (capture_layer(*g, c, x, w, bias, gamma, out, topk_idx, topk_gate, counts, max_over_mean, ws) !=
+              MOE_OK)
+            g->failed = true;
+        }
+        if (g->exec != nullptr) {
+          const moe_status r = replay_layer(*g, st);
+          if (r == MOE_OK) return MOE_OK;
+          g->failed = true;  // run this call eagerly below
+          (void)cudaGetLastError();
+        }
+      }
+    }
+  }
+  return layer_forward_body(c, x, w, bias, gamma, out, topk_idx, topk_gate, counts, max_over_mean, ws, st);
+}
+
+moe_status moe_set_layer_graphs(int enable) {
+  if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  g_graphs_mode = enable;
+  return MOE_OK;
+}
+
+moe_status moe_layer_graphs_kept(int* n) {
+  if (n == nullptr) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  int c = 0;
+  for (const LayerGraph& e : *g_graphs) c += e.exec != nullptr;
+  *n = c;
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status layer_forward_body(const moe_config& c, const void* x, const moe_weights* w, float* bias, float gamma,
+                              void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts, float* max_over_mean,
+                              void* ws, cudaStream_t st) {
   const Layout Lw = layout(c);
   MOE_TRY(stage_mark(0, st));
   MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
@@ -275,6 +503,10 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const moe_wei
   }
   return MOE_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 moe_status moe_quantize_weights_e4m3(const void* w, int n_mat, int rows, int cols, uint8_t* q, float* scale,
                                      moe_stream_t stream) {

@@ -122,6 +122,10 @@ def test_newer_entry_points_reject_bad_arguments_before_any_cuda_call():
     assert B.lib.moe_set_stage_events(arr, 4) == 1
     arr8 = (ctypes.c_void_p * 8)(*([0x10] * 7 + [None]))
     assert B.lib.moe_set_stage_events(arr8, 8) == 1
+    # graph replay toggle: on / off only
+    assert B.lib.moe_set_layer_graphs(2) == 1
+    assert B.lib.moe_set_layer_graphs(0) == 0 and B.lib.moe_set_layer_graphs(1) == 0
+    assert B.lib.moe_layer_graphs_kept(None) == 1 and B.moe_layer_graphs_kept() == 0
     # device error query needs a workspace and an output
     code = ctypes.c_int(0)
     assert B.lib.moe_device_error(None, None, ctypes.byref(code)) == 1
