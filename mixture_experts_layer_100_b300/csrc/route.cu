@@ -13,6 +13,13 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// Groups of exactly 32 experts (one register of every lane) with the sum of
+// at most the 2 largest biased affinities: the group scores are formed by a
+// warp butterfly on registers, without the shared-memory copy of s'.
+__host__ __device__ __forceinline__ bool butterfly_groups(int E, int G, int gk, int npl) {
+  return G > 0 && E == 32 * G && npl == G && gk <= 2;
+}
+
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -46,63 +53,100 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     const float* srow = scores + (size_t)t * E;
     float s[NPL], v[NPL];
+    const bool fly = butterfly_groups(E, G, gk, NPL);
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
       const int e = lane + 32 * j;
       s[j] = e < E ? srow[e] : 0.0f;
       v[j] = __fadd_rn(s[j], b[j]);  // s' = s + b, one fp32 add
-      if (e < E) sp[e] = v[j];
+      if (!fly && e < E) sp[e] = v[j];
     }
     __syncwarp();
 
-    // group score: sum of the gk largest s' of the group, largest first
-    float gs = -INFINITY;
-    if (lane < G) {
-      const float* grp = sp + lane * gsz;
-      if (gk <= 4) {
-        float top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        for (int j = 0; j < gsz; ++j) {
-          float x = grp[j];
+    unsigned gmask = 0;
+    if (fly) {
+      // group j = register j of all lanes: top-2 of the group by a butterfly
+      // (every lane ends with every group's two largest values)
+      float t1[NPL], t2[NPL];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            if (r < gk && x > top[r]) {
-              const float tmp = top[r];
-              top[r] = x;
-              x = tmp;
-            }
-          }
-        }
-        gs = top[0];
-        for (int r = 1; r < gk; ++r) gs = __fadd_rn(gs, top[r]);
-      } else {
-        // larger gk (up to the whole group, the plain node sum): take the
-        // members in (value desc, index asc) order one at a time
-        float last_v = INFINITY;
-        int last_j = -1;
-        for (int r = 0; r < gk; ++r) {
-          float bv = -INFINITY;
-          int bj = gsz;
-          for (int j = 0; j < gsz; ++j) {
-            const float x = grp[j];
-            const bool after_last = x < last_v || (x == last_v && j > last_j);
-            if (after_last && (x > bv || (x == bv && j < bj))) {
-              bv = x;
-              bj = j;
-            }
-          }
-          gs = r == 0 ? bv : __fadd_rn(gs, bv);
-          last_v = bv;
-          last_j = bj;
+      for (int j = 0; j < NPL; ++j) {
+        t1[j] = v[j];
+        t2[j] = -INFINITY;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+          const float p1 = __shfl_xor_sync(0xffffffffu, t1[j], o);
+          const float p2 = __shfl_xor_sync(0xffffffffu, t2[j], o);
+          const float hi = t1[j] > p1 ? t1[j] : p1;
+          const float lo = t1[j] > p1 ? p1 : t1[j];
+          const float m2 = t2[j] > p2 ? t2[j] : p2;
+          t2[j] = lo > m2 ? lo : m2;
+          t1[j] = hi;
         }
       }
+      float gsa[NPL];
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) gsa[j] = gk == 1 ? t1[j] : __fadd_rn(t1[j], t2[j]);
+      // the M best groups (ties: lower group index), computed by every lane
+#pragma unroll
+      for (int g = 0; g < NPL; ++g) {
+        int rank = 0;
+#pragma unroll
+        for (int g2 = 0; g2 < NPL; ++g2) rank += (gsa[g2] > gsa[g]) || (gsa[g2] == gsa[g] && g2 < g);
+        if (rank < M) gmask |= 1u << g;
+      }
+    } else {
+      // group score: sum of the gk largest s' of the group, largest first
+      float gs = -INFINITY;
+      if (lane < G) {
+        const float* grp = sp + lane * gsz;
+        if (gk <= 4) {
+          float top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          for (int j = 0; j < gsz; ++j) {
+            float x = grp[j];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              if (r < gk && x > top[r]) {
+                const float tmp = top[r];
+                top[r] = x;
+                x = tmp;
+              }
+            }
+          }
+          gs = top[0];
+          for (int r = 1; r < gk; ++r) gs = __fadd_rn(gs, top[r]);
+        } else {
+          // larger gk (up to the whole group, the plain node sum): take the
+          // members in (value desc, index asc) order one at a time
+          float last_v = INFINITY;
+          int last_j = -1;
+          for (int r = 0; r < gk; ++r) {
+            float bv = -INFINITY;
+            int bj = gsz;
+            for (int j = 0; j < gsz; ++j) {
+              const float x = grp[j];
+              const bool after_last = x < last_v || (x == last_v && j > last_j);
+              if (after_last && (x > bv || (x == bv && j < bj))) {
+                bv = x;
+                bj = j;
+              }
+            }
+            gs = r == 0 ? bv : __fadd_rn(gs, bv);
+            last_v = bv;
+            last_j = bj;
+          }
+        }
+      }
+      // the M best groups (ties: lower group index)
+      int rank = 0;
+      for (int g2 = 0; g2 < G; ++g2) {
+        const float o = __shfl_sync(0xffffffffu, gs, g2);
+        rank += (o > gs) || (o == gs && g2 < lane);
+      }
+      gmask = __ballot_sync(0xffffffffu, lane < G && rank < M);
     }
-    // the M best groups (ties: lower group index)
-    int rank = 0;
-    for (int g2 = 0; g2 < G; ++g2) {
-      const float o = __shfl_sync(0xffffffffu, gs, g2);
-      rank += (o > gs) || (o == gs && g2 < lane);
-    }
-    const unsigned gmask = __ballot_sync(0xffffffffu, lane < G && rank < M);
 
     uint64_t key[NPL];
 #pragma unroll
@@ -233,7 +277,10 @@ cudaError_t launch_seq_balance(const float* scores, const int* topk_idx, int T, 
 cudaError_t launch_route_select(const float* scores, const float* bias, int T, int E, int G, int K, int M, int gk,
                                 int* topk_idx, float* topk_gate, int* counts, int num_sms, cudaStream_t st) {
   const int npl = (E + 31) / 32;
-  const size_t smem = (size_t)(E + kWarps * E) * sizeof(float);
+  // the histogram, and (unless the group scores come from the butterfly)
+  // each warp's copy of s'
+  const int npl_k = npl <= 8 ? npl : npl <= 12 ? 12 : 16;  // the instantiation that runs
+  const size_t smem = (size_t)(E + (butterfly_groups(E, G, gk, npl_k) ? 0 : kWarps * E)) * sizeof(float);
   const int blocks = std::max(1, std::min((T + kWarps - 1) / kWarps, num_sms * 4));
 #define MOE_ROUTE_CASE(N)                                                                         \
   case N:                                                                                         \
